@@ -1,0 +1,213 @@
+"""Plain restatement of FCP's block distributor and work list (oracle; test infrastructure).
+
+Source: "Unleashing Scalable Context Parallelism for Foundation Models
+Pre-Training via FCP" (arXiv 2605.08524):
+
+* Section 3.3 (problem formulation): a sharding function G maps each sequence to
+  blocks, an assignment function M maps each block to a worker, and a worker's
+  load is the sum of f(B) over its blocks.
+* Section 4.1 (block distributor, sharding policy): every sequence is cut into
+  fixed-size blocks; sequences shorter than the block size are packed into the
+  fewest blocks and computed with the varlen kernel interface.
+* Section 3.2 / Figure 4 (Zig-Zag): for a causal sequence, block i is paired with
+  the block at the mirrored position so that every pair carries equal compute.
+* Sections 3.2 and 4.1 (assignment policy): a variant of Longest Processing Time
+  greedily gives each block to the least-loaded worker, under a strict cap on the
+  tokens a worker holds.
+* Section 4.2 (bottom-up coalescer): consecutive block-level sub-stages of a
+  worker can be merged into one execution stage of up to c blocks.
+
+Readings where the pages are silent (Appendix A.1 is not on the pages):
+
+1. Blocks: a sequence of length L >= b gives ceil(L/b) blocks aligned at its
+   start; a short final block stays its own block. L == b is one full block.
+2. Packing of L < b: First-Fit-Decreasing by length (ties: lower sequence index),
+   bins in creation order, segments in insertion order. FFD is not always the
+   minimum; the pages' "minimal number of blocks" is bin packing.
+3. Block order: unpacked sequences in input order (blocks in order), then bins.
+4. Zig-Zag partner of block j of a causal sequence of k blocks: k-1-j (0-based);
+   the middle block of an odd k and every packed or full-mask block has none (-1).
+   The pages' "i-th with (2N-i)-th" is off by one under either indexing.
+5. Cost f(B): unmasked score pairs whose query lies in B. Causal segment at
+   offset s of length l: s*l + l(l+1)/2; full mask: l * L_seq. The efficiency
+   factor is constant at a fixed block size and is dropped.
+6. LPT: blocks by cost descending, ties by block id ascending; each goes to the
+   least-loaded worker among those whose tokens + len(B) <= cap, ties by lowest
+   worker id. No such worker: capacity error. Default cap: b * ceil(K / N).
+7. Work list, per worker, per owned Q-block (ascending id), per segment: an
+   unpacked causal block j of a sequence pairs with KV blocks 0..j of it (j is the
+   causal diagonal, the rest full); full mask pairs with every block of the
+   sequence; a packed segment pairs with itself.
+8. Runs (coalescing): consecutive items of one worker with the same query range,
+   at most c per run; each run owns one partial (O, LSE) slot.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence
+
+FULL = 0
+CAUSAL_DIAG = 1
+
+
+class CapacityError(Exception):
+    """No worker can take a block without exceeding the token cap."""
+
+
+def segment_cost(start: int, length: int, seq_len: int, causal: bool) -> int:
+    """Unmasked score pairs of the queries at positions [start, start+length) of a sequence."""
+    if causal:
+        return sum(i + 1 for i in range(start, start + length))
+    return length * seq_len
+
+
+def partition(seqlens: Sequence[int], block_size: int, causal: bool) -> Dict[str, list]:
+    """Sharding G with packing and Zig-Zag partners.
+
+    Returns blocks as tuples (first_seg, n_segs, tokens, seq, seq_block_idx,
+    seq_nblocks, zz_partner, cost) -- seq is -1 for a packed block -- and segments
+    as tuples (seq, start_in_seq, length, tok0), tok0 being the segment's offset in
+    the packed token order of the input.
+    """
+    if block_size <= 0:
+        raise ValueError("block size must be positive")
+    if any(L < 0 for L in seqlens):
+        raise ValueError("negative sequence length")
+    seq_start = [0] * len(seqlens)
+    acc = 0
+    for i, L in enumerate(seqlens):
+        seq_start[i] = acc
+        acc += L
+
+    blocks: List[tuple] = []
+    segs: List[tuple] = []
+    # unpacked sequences, in input order
+    for i, L in enumerate(seqlens):
+        if L < block_size:
+            continue
+        k = -(-L // block_size)
+        for j in range(k):
+            start = j * block_size
+            ln = min(block_size, L - start)
+            partner = (k - 1 - j) if (causal and k - 1 - j != j) else -1
+            cost = segment_cost(start, ln, L, causal)
+            blocks.append((len(segs), 1, ln, i, j, k, partner, cost))
+            segs.append((i, start, ln, seq_start[i] + start))
+
+    # short sequences: first-fit-decreasing into bins of block_size tokens
+    short = [i for i, L in enumerate(seqlens) if 0 < L < block_size]
+    short.sort(key=lambda i: (-seqlens[i], i))
+    bins: List[List[int]] = []
+    room: List[int] = []
+    for i in short:
+        for bi in range(len(bins)):
+            if room[bi] >= seqlens[i]:
+                bins[bi].append(i)
+                room[bi] -= seqlens[i]
+                break
+        else:
+            bins.append([i])
+            room.append(block_size - seqlens[i])
+    for members in bins:
+        first = len(segs)
+        tokens = 0
+        cost = 0
+        for i in members:
+            L = seqlens[i]
+            segs.append((i, 0, L, seq_start[i]))
+            tokens += L
+            cost += segment_cost(0, L, L, causal)
+        blocks.append((first, len(members), tokens, -1, 0, 1, -1, cost))
+    return {"blocks": blocks, "segs": segs, "seqlens": list(seqlens), "block_size": block_size,
+            "causal": causal}
+
+
+def default_cap(n_blocks: int, n_workers: int, block_size: int) -> int:
+    return block_size * (-(-n_blocks // n_workers)) if n_blocks else block_size
+
+
+def distribute(part: Dict[str, list], n_workers: int, token_cap: Optional[int] = None) -> Dict[str, list]:
+    """Assignment M (LPT under a token cap) and the work list of (Q, KV, mask) items.
+
+    Returns worker_of_block, load (sum of block costs per worker), tokens per
+    worker, the cap used, and items as tuples
+    (worker, q_block, kv_block, q_tok0, q_len, kv_tok0, kv_len, mask).
+    """
+    if n_workers <= 0:
+        raise ValueError("need at least one worker")
+    blocks, segs = part["blocks"], part["segs"]
+    K = len(blocks)
+    cap = token_cap if (token_cap is not None and token_cap > 0) else default_cap(K, n_workers, part["block_size"])
+    order = sorted(range(K), key=lambda b: (-blocks[b][7], b))
+    load = [0] * n_workers
+    tokens = [0] * n_workers
+    owner = [-1] * K
+    for b in order:
+        need = blocks[b][2]
+        best = -1
+        for w in range(n_workers):
+            if tokens[w] + need > cap:
+                continue
+            if best < 0 or load[w] < load[best]:
+                best = w
+        if best < 0:
+            raise CapacityError(f"block {b} ({need} tokens) fits no worker under cap {cap}")
+        owner[b] = best
+        load[best] += blocks[b][7]
+        tokens[best] += need
+
+    # blocks of each unpacked sequence, by position
+    seq_blocks: Dict[int, List[int]] = {}
+    for b, blk in enumerate(blocks):
+        if blk[3] >= 0:
+            seq_blocks.setdefault(blk[3], []).append(b)
+
+    causal = part["causal"]
+    items: List[tuple] = []
+    for w in range(n_workers):
+        for qb in range(K):
+            if owner[qb] != w:
+                continue
+            first, nseg, _, seq, j, _, _, _ = blocks[qb]
+            for si in range(first, first + nseg):
+                _, _, qlen, qtok = segs[si]
+                if seq < 0:  # packed segment: attends to itself only
+                    items.append((w, qb, qb, qtok, qlen, qtok, qlen, CAUSAL_DIAG if causal else FULL))
+                    continue
+                kv_list = seq_blocks[seq][: j + 1] if causal else seq_blocks[seq]
+                for kb in kv_list:
+                    kseg = segs[blocks[kb][0]]
+                    mask = CAUSAL_DIAG if (causal and kb == qb) else FULL
+                    items.append((w, qb, kb, qtok, qlen, kseg[3], kseg[2], mask))
+    return {"worker_of_block": owner, "load": load, "tokens": tokens, "cap": cap, "items": items}
+
+
+def coalesce(items: Sequence[tuple], degree: int) -> List[tuple]:
+    """Runs of at most `degree` consecutive items of one worker sharing a query range.
+
+    Returns runs as tuples (worker, q_block, q_tok0, q_len, item_begin, item_end,
+    part_row0), part_row0 being the run's first row in the partial-result buffer
+    (runs laid end to end, q_len rows each).
+    """
+    if degree <= 0:
+        raise ValueError("coalesce degree must be positive")
+    runs: List[tuple] = []
+    row = 0
+    i = 0
+    while i < len(items):
+        w, qb, _, qtok, qlen = items[i][:5]
+        j = i + 1
+        while (j < len(items) and j - i < degree and items[j][0] == w
+               and items[j][3] == qtok and items[j][4] == qlen):
+            j += 1
+        runs.append((w, qb, qtok, qlen, i, j, row))
+        row += qlen
+        i = j
+    return runs
+
+
+def imbalance(load: Sequence[int]) -> float:
+    """(max(load) - mean(load)) / max(load), the pages' imbalance ratio (Section 6.2)."""
+    mx = max(load)
+    if mx == 0:
+        return 0.0
+    return (mx - sum(load) / len(load)) / mx
