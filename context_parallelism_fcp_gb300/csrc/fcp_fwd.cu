@@ -1,0 +1,410 @@
+// Forward block attention over the FCP work list on sm_103a (tcgen05 + TMEM + TMA).
+//
+// Computes, for every run (a query range with up to c work items, "Unleashing Scalable
+// Context Parallelism for Foundation Models Pre-Training via FCP", Section 4.2 coalescer) and
+// every query head, the attention of Section 2.2 over the run's key ranges, written as a
+// partial (O normalised over those keys, natural LSE) -- the per-slice partial results of
+// Section 2.3 that the merge reduces.
+//
+// CTA = one 128-row query tile of one run, for two query heads of the same KV group (two
+// "tiles" t = 0, 1 that share every K/V tile loaded into shared memory). 10 warps:
+//   warps 0-3  softmax of tile 0: thread = query row = TMEM lane
+//   warps 4-7  softmax of tile 1
+//   warp  8    TMA producer: Q tiles once, then K and V tiles through 2-stage rings
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM (512 columns x 128 lanes, fp32): S_t at columns [128t, 128t+128), O_t at
+// [256+128t, 256+128t+D). Softmax overwrites S_t's first 64 columns with P_t as packed bf16;
+// O_t += P_t V runs with A read from TMEM. Per key tile the issue order is
+// PV(0,j-1), S(0,j), PV(1,j-1), S(1,j), so the tensor core works on one tile while the other
+// tile's softmax runs. O is rescaled lazily: only when a row maximum grows by more than
+// 2^8 (in exp2 units), keeping every P <= 256; the final normalisation uses the same stale
+// maximum, so the result is exact up to rounding.
+#include "fcp_cuda_util.h"
+#include "fcp_sm100.cuh"
+
+namespace fcp {
+namespace {
+
+using namespace dev;
+
+constexpr int kFwdThreads = 320;
+constexpr int kPanelBytes = kTileM * 128;  // one box: 128 rows x 64 bf16 channels
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+struct FwdArgs {
+  const fcp_item* items;
+  const fcp_run* runs;
+  const FwdUnit* units;
+  float* part_o;
+  float* part_lse;
+  long long part_rows;
+  int hq, hkv, group, pairs_per_group;
+  float scale_log2;
+  int* err;
+};
+
+enum : int {
+  B_QFULL = 0,
+  B_KFULL = 1,   // 2 stages
+  B_KEMPTY = 3,  // 2 stages
+  B_VFULL = 5,
+  B_VEMPTY = 7,
+  B_SFULL = 9,   // per tile
+  B_PFULL = 11,  // per tile
+  B_ODONE = 13,  // per tile
+  B_DRAIN = 15,
+  B_COUNT = 16
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = kTileM * D * 2;
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kTileBytes;
+  static constexpr int kK = 2 * kTileBytes;
+  static constexpr int kV = 4 * kTileBytes;
+  static constexpr int kBar = 6 * kTileBytes;
+  // at least half the SM's shared memory, so one CTA per SM holds all 512 TMEM columns
+  static constexpr int kSmemBytes = (kBar + 256) > 118 * 1024 ? (kBar + 256) : 118 * 1024;
+  static constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16(kTileM, D, false, true);
+};
+
+__device__ __forceinline__ int kv_tiles(const fcp_item& it, int q_tile) {
+  int n = (it.kv_len + kTileN - 1) / kTileN;
+  if (it.mask == FCP_MASK_CAUSAL_DIAG) n = min(n, q_tile + 1);
+  return n;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte-swizzled TMA/MMA tiles need a 1024-byte aligned base; report, never fault
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, kErrSmemAlign);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  const uint32_t sb = smem_u32(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kBar + B_COUNT * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBar + B_COUNT * 8 + 4);
+  auto bar = [&](int i) -> uint32_t { return sb + C::kBar + 8 * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int per_unit = a.hkv * a.pairs_per_group;
+  const int unit_idx = blockIdx.x / per_unit;
+  const int rem = blockIdx.x - unit_idx * per_unit;
+  const int kvh = rem / a.pairs_per_group;
+  const int pair = rem - kvh * a.pairs_per_group;
+  const int h0 = kvh * a.group + 2 * pair;
+  const bool has_h1 = 2 * pair + 1 < a.group;
+  const int h1 = has_h1 ? h0 + 1 : h0;
+  const FwdUnit unit = a.units[unit_idx];
+  const fcp_run run = a.runs[unit.run];
+  const int qt = unit.q_tile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_PFULL + s), kTileM);
+      mbar_init(bar(B_ODONE + s), 1);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
+    mbar_fence_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = *abort_flag != 0;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && !skip) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int qrow = run.q_tok0 + qt * kTileM;
+      mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::kTileBytes);
+#pragma unroll
+      for (int p = 0; p < C::kPanels; ++p) {
+        tma_load_3d(sb + C::kQ0 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, h0);
+        tma_load_3d(sb + C::kQ1 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, h1);
+      }
+      int j = 0;
+      bool ok = true;
+      for (int ii = run.item_begin; ii < run.item_end && ok; ++ii) {
+        const fcp_item itm = a.items[ii];
+        const int nkt = kv_tiles(itm, qt);
+        for (int kt = 0; kt < nkt; ++kt, ++j) {
+          const int s = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          const int kvrow = itm.kv_tok0 + kt * kTileN;
+          if (!mbar_wait(bar(B_KEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_KFULL + s), C::kTileBytes);
+#pragma unroll
+          for (int p = 0; p < C::kPanels; ++p)
+            tma_load_3d(sb + C::kK + s * C::kTileBytes + p * kPanelBytes, &tmK, bar(B_KFULL + s), p * 64, kvrow, kvh);
+          if (!mbar_wait(bar(B_VEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 2)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_VFULL + s), C::kTileBytes);
+#pragma unroll
+          for (int p = 0; p < C::kPanels; ++p)
+            tma_load_3d(sb + C::kV + s * C::kTileBytes + p * kPanelBytes, &tmV, bar(B_VFULL + s), p * 64, kvrow, kvh);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && !skip) {
+      auto issue_s = [&](int t, int s) {
+        const uint32_t d = tmem + t * 128;
+        const uint32_t qbase = sb + (t ? C::kQ1 : C::kQ0);
+        const uint32_t kbase = sb + C::kK + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+          mma_ss(d, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::kIdescS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int s, bool acc) {
+        const uint32_t d = tmem + 256 + t * 128;
+        const uint32_t p = tmem + t * 128;
+        const uint32_t vbase = sb + C::kV + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts(d, p + kk * 8, sdesc_sw128(vbase + kk * 2048, kPanelBytes, 1024), C::kIdescPV, (acc || kk > 0));
+      };
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.err, kErrFwdWait + 3);
+      tc_fence_after();
+      int j = 0;
+      for (int ii = run.item_begin; ii < run.item_end && ok; ++ii) {
+        const fcp_item itm = a.items[ii];
+        const int nkt = kv_tiles(itm, qt);
+        for (int kt = 0; kt < nkt && ok; ++kt, ++j) {
+          const int s = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!mbar_wait(bar(B_KFULL + s), ph, abort_flag, a.err, kErrFwdWait + 4)) { ok = false; break; }
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t) {
+            if (j > 0) {
+              const int ps = (j - 1) & 1;
+              if (t == 0) {
+                if (!mbar_wait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, abort_flag, a.err, kErrFwdWait + 5)) {
+                  ok = false;
+                  break;
+                }
+              }
+              if (!mbar_wait(bar(B_PFULL + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 6)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_pv(t, ps, j - 1 > 0);
+              tc_commit(bar(B_ODONE + t));
+              if (t == 1) tc_commit(bar(B_VEMPTY + ps));
+            }
+            issue_s(t, s);
+            tc_commit(bar(B_SFULL + t));
+          }
+          if (ok) tc_commit(bar(B_KEMPTY + s));
+        }
+      }
+      if (ok && j > 0) {
+        const int ps = (j - 1) & 1;
+        ok = mbar_wait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, abort_flag, a.err, kErrFwdWait + 5);
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = mbar_wait(bar(B_PFULL + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 6);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, ps, j - 1 > 0);
+          tc_commit(bar(B_ODONE + t));
+        }
+      }
+      // every issued MMA has completed once the drain barrier fires
+      tc_commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0, abort_flag, a.err, kErrFwdWait + 7);
+    }
+  } else if (!skip) {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int t = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_addr = lane_base + t * 128;
+    const uint32_t o_addr = lane_base + 256 + t * 128;
+    float m_used = -INFINITY;
+    float l = 0.f;
+    int j = 0;
+    bool ok = true;
+    for (int ii = run.item_begin; ii < run.item_end && ok; ++ii) {
+      const fcp_item itm = a.items[ii];
+      const int nkt = kv_tiles(itm, qt);
+      for (int kt = 0; kt < nkt; ++kt, ++j) {
+        const int kv_valid = itm.kv_len - kt * kTileN;
+        const bool diag = itm.mask == FCP_MASK_CAUSAL_DIAG && kt == qt;
+        const int lim = diag ? min(r + 1, kv_valid) : kv_valid;  // visible key columns [0, lim)
+        ok = mbar_wait(bar(B_SFULL + t), j & 1, abort_flag, a.err, kErrFwdWait + 8);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv[c]);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(sv[c][e]));
+        const float m_new = fmaxf(m_used, mx * a.scale_log2);
+        float alpha = 1.f;
+        const bool grow = m_new > m_used + kRescaleThreshold;
+        if (grow) {
+          alpha = fast_exp2(m_used - m_new);
+          m_used = m_new;
+        }
+        const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+        float rowsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = c * 32 + 2 * e;
+            const float p0 = (c0 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c][2 * e]), a.scale_log2, -mb)) : 0.f;
+            const float p1 = (c0 + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c][2 * e + 1]), a.scale_log2, -mb)) : 0.f;
+            rowsum += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tmem_st16(s_addr + c * 16, pk);
+        }
+        l = l * alpha + rowsum;
+        // O holds the sum through key tile j-1 once PV(t, j-1) completes; rows whose maximum
+        // grew are rescaled before PV(t, j) adds onto it (warp-uniform TMEM access).
+        if (__any_sync(0xffffffffu, grow && j > 0)) {
+          ok = mbar_wait(bar(B_ODONE + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 9);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_addr + c * 32, ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(o_addr + c * 32, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_PFULL + t));
+      }
+    }
+    if (ok && j > 0) {
+      ok = mbar_wait(bar(B_ODONE + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 10);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const int qrow = qt * kTileM + r;
+        const bool store = qrow < run.q_len && (t == 0 || has_h1);
+        const int h = t ? h1 : h0;
+        const long long prow = static_cast<long long>(h) * a.part_rows + run.part_row0 + qrow;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_addr + c * 32, ov);
+          if (store) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[c * 8 + e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
+                                           __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+          }
+        }
+        if (store) a.part_lse[prow] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  if (*abort_flag) {
+    // let in-flight asynchronous copies land before the CTA's shared memory is released
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 1000000ull) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+fcp_status launch_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
+                      int hq, int hkv, float* part_o, float* part_lse, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  const DevLayout& L = plan->layout;
+  if (L.n_fwd_units == 0) return FCP_OK;
+  const int64_t T = plan->total_tokens;
+  CUtensorMap mq, mk, mv;
+  fcp_status st;
+  if ((st = make_bf16_map(&mq, q, hq, T, D, kTileM)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mk, k, hkv, T, D, kTileN)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mv, v, hkv, T, D, kTileN)) != FCP_OK) return st;
+  FwdArgs a;
+  a.items = dev_array<fcp_item>(d_plan, L.items);
+  a.runs = dev_array<fcp_run>(d_plan, L.runs);
+  a.units = dev_array<FwdUnit>(d_plan, L.fwd_units);
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.part_rows = plan->partial_rows;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.group = hq / hkv;
+  a.pairs_per_group = (a.group + 1) / 2;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  a.err = dev_error_word(d_plan);
+  FCP_CUDA_TRY(cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
+               "fwd smem attribute");
+  const long long grid = static_cast<long long>(L.n_fwd_units) * hkv * a.pairs_per_group;
+  if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
+  fwd_kernel<D><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
+  FCP_CUDA_TRY(cudaGetLastError(), "fwd launch");
+  return FCP_OK;
+}
+
+}  // namespace
+}  // namespace fcp
+
+using namespace fcp;
+
+extern "C" fcp_status fcp_block_attn_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
+                                         const void* v, int32_t hq, int32_t hkv, int32_t head_dim, float* part_o,
+                                         float* part_lse, void* stream) {
+  if (plan == nullptr || d_plan == nullptr) return FCP_ERR_INVALID;
+  if (!plan->distributed) return FCP_ERR_STATE;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return FCP_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return FCP_ERR_UNSUPPORTED;
+  if (plan->layout.n_fwd_units == 0) return FCP_OK;
+  if (!q || !k || !v || !part_o || !part_lse) return FCP_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(part_o)) return FCP_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (head_dim == 128) return launch_fwd<128>(plan, d_plan, q, k, v, hq, hkv, part_o, part_lse, s);
+  return launch_fwd<64>(plan, d_plan, q, k, v, hq, hkv, part_o, part_lse, s);
+}

@@ -1,0 +1,85 @@
+// Internal definitions shared by the host plan (fcp_plan.cpp) and the device entry points
+// (*.cu): the host plan object and the layout of its device image.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "fcp.h"
+
+namespace fcp {
+
+// Tile shape of the attention kernels: 128 query rows x 128 key rows. 128 is the M of one
+// single-CTA tcgen05.mma and the number of TMEM lanes, so one thread owns one row.
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+
+// A query range with its runs (consecutive in the run list): what the merge reduces.
+struct QSeg {
+  int32_t tok0, len, run_begin, run_end;
+};
+// One forward CTA's work: query tile q_tile of run `run`.
+struct FwdUnit {
+  int32_t run, q_tile;
+};
+// A key range with the items that read it (indices into kv_items[list_begin, list_end)).
+struct KvSeg {
+  int32_t tok0, len, list_begin, list_end;
+};
+// One backward CTA's work: key tile kv_tile of key range `kvseg`.
+struct BwdUnit {
+  int32_t kvseg, kv_tile;
+};
+
+// Header at offset 0 of the device image. error: 0, or the code of the first device-side
+// failure (a bounded wait that gave up); see fcp_device_error.
+struct DevHeader {
+  int32_t error;
+  int32_t error_info;
+  int32_t reserved[62];
+};
+static_assert(sizeof(DevHeader) == 256, "header is one 256-byte line");
+
+// Byte offsets of the arrays in the device image and their lengths.
+struct DevLayout {
+  size_t items = 0, runs = 0, qsegs = 0, tok2qseg = 0, fwd_units = 0, kvsegs = 0, kv_items = 0,
+         bwd_units = 0, total = 0;
+  int32_t n_qsegs = 0, n_fwd_units = 0, n_kvsegs = 0, n_kv_items = 0, n_bwd_units = 0;
+  int32_t max_runs_per_qseg = 0;
+};
+
+// Device error codes written into DevHeader::error (kernel id * 16 + wait id).
+enum DevError : int32_t {
+  kErrSmemAlign = 0x01,
+  kErrFwdWait = 0x10,
+  kErrBwdWait = 0x20,
+};
+
+void set_last_error(const std::string& msg);
+
+}  // namespace fcp
+
+struct fcp_plan {
+  std::vector<int32_t> seqlens;
+  int32_t block_size = 0;
+  int32_t causal = 0;
+  int64_t total_tokens = 0;
+  int64_t total_pairs = 0;
+  std::vector<fcp_block> blocks;
+  std::vector<fcp_segment> segs;
+
+  bool distributed = false;
+  int32_t n_workers = 0;
+  int64_t token_cap = 0;
+  int32_t coalesce = 1;
+  std::vector<int64_t> load, tokens;
+  std::vector<fcp_item> items;
+  std::vector<fcp_run> runs;
+  int64_t partial_rows = 0;
+
+  // Host copy of the device image, rebuilt after distribute/coalesce.
+  std::vector<uint8_t> image;
+  fcp::DevLayout layout;
+};

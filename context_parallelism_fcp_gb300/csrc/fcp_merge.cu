@@ -1,0 +1,266 @@
+// Bandwidth-bound kernels of the hot path and the device-image entry points:
+//   - the associative log-sum-exp merge of partial results ("Unleashing Scalable Context
+//     Parallelism for Foundation Models Pre-Training via FCP", Section 2.3: partial results
+//     over slices of L reduced to the final output);
+//   - the backward prologue Di = rowsum(dO * O), fused with zeroing the dQ accumulator;
+//   - the dQ conversion (scale, float32 -> bf16);
+//   - fcp_plan_upload / fcp_device_error.
+// One warp handles one (head, token) row of D channels: lane l owns channels
+// [l*D/32, (l+1)*D/32), so every global access of a warp is one contiguous span.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "fcp_cuda_util.h"
+
+namespace fcp {
+namespace {
+
+constexpr int kRowWarps = 8;  // warps (rows) per 256-thread block
+
+template <int D>
+struct Vec;
+template <>
+struct Vec<128> {
+  using F = float4;
+  static constexpr int N = 4;
+};
+template <>
+struct Vec<64> {
+  using F = float2;
+  static constexpr int N = 2;
+};
+
+__device__ __forceinline__ void vload(const float4* p, float (&x)[4]) {
+  const float4 v = __ldg(p);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+__device__ __forceinline__ void vload(const float2* p, float (&x)[2]) {
+  const float2 v = __ldg(p);
+  x[0] = v.x; x[1] = v.y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// grid (ceil(T / kRowWarps), Hq); warp w of block x handles token x*kRowWarps + w of head y.
+template <int D>
+__global__ void __launch_bounds__(32 * kRowWarps)
+    merge_kernel(const QSeg* __restrict__ qsegs, const int* __restrict__ tok2qseg, const fcp_run* __restrict__ runs,
+                 const float* __restrict__ part_o, const float* __restrict__ part_lse, long long part_rows,
+                 long long T, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  using V = Vec<D>;
+  constexpr int N = V::N;
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int h = blockIdx.y;
+  const QSeg qs = qsegs[tok2qseg[t]];
+  const int row = static_cast<int>(t - qs.tok0);
+  const long long head_base = static_cast<long long>(h) * part_rows + row;
+  const int nr = qs.run_end - qs.run_begin;
+
+  // max of the partial LSEs, lanes striding over runs
+  float m = -INFINITY;
+  for (int i = lane; i < nr; i += 32) m = fmaxf(m, __ldg(part_lse + head_base + runs[qs.run_begin + i].part_row0));
+  m = warp_max(m);
+
+  float acc[N];
+#pragma unroll
+  for (int e = 0; e < N; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int base = 0; base < nr; base += 32) {
+      // each lane fetches one run's weight and row offset, then the warp walks them
+      float w_l = 0.f;
+      long long off_l = 0;
+      if (base + lane < nr) {
+        const long long pr = head_base + runs[qs.run_begin + base + lane].part_row0;
+        w_l = __expf(__ldg(part_lse + pr) - m);
+        off_l = pr;
+      }
+      const int cnt = min(32, nr - base);
+#pragma unroll 4
+      for (int i = 0; i < cnt; ++i) {
+        const float w = __shfl_sync(0xffffffffu, w_l, i);
+        const long long pr = __shfl_sync(0xffffffffu, off_l, i);
+        float x[N];
+        vload(reinterpret_cast<const typename V::F*>(part_o + pr * D) + lane, x);
+#pragma unroll
+        for (int e = 0; e < N; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+        wsum += w;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = o + (static_cast<long long>(h) * T + t) * D + lane * N;
+  if constexpr (N == 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&a);
+    pk.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0) lse[static_cast<long long>(h) * T + t] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
+// Di[h,t] = sum_d dO*O and dq_acc[h,t,:] = 0. grid (ceil(T / kRowWarps), Hq).
+template <int D>
+__global__ void __launch_bounds__(32 * kRowWarps)
+    prologue_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, long long T,
+                    float* __restrict__ di, float* __restrict__ dq_acc) {
+  constexpr int N = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const long long row = static_cast<long long>(blockIdx.y) * T + t;
+  const __nv_bfloat16* po = o + row * D + lane * N;
+  const __nv_bfloat16* pd = dout + row * D + lane * N;
+  float s = 0.f;
+  if constexpr (N == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(po);
+    const uint2 b = *reinterpret_cast<const uint2*>(pd);
+    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+    const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+    const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
+    const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
+    s = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+    reinterpret_cast<float4*>(dq_acc + row * D)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(po));
+    const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pd));
+    s = a0.x * b0.x + a0.y * b0.y;
+    reinterpret_cast<float2*>(dq_acc + row * D)[lane] = make_float2(0.f, 0.f);
+  }
+  s = warp_sum(s);
+  if (lane == 0) di[row] = s;
+}
+
+// dq[i] = bf16(scale * dq_acc[i]), 8 elements per thread, grid-stride.
+__global__ void __launch_bounds__(256)
+    dq_convert_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, long long n8, float scale) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+    __nv_bfloat162 r0 = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+    __nv_bfloat162 r1 = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+    __nv_bfloat162 r2 = __floats2bfloat162_rn(b.x * scale, b.y * scale);
+    __nv_bfloat162 r3 = __floats2bfloat162_rn(b.z * scale, b.w * scale);
+    uint4 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&r0);
+    pk.y = *reinterpret_cast<uint32_t*>(&r1);
+    pk.z = *reinterpret_cast<uint32_t*>(&r2);
+    pk.w = *reinterpret_cast<uint32_t*>(&r3);
+    reinterpret_cast<uint4*>(dq)[i] = pk;
+  }
+}
+
+}  // namespace
+
+fcp_status launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale, cudaStream_t s) {
+  if (n == 0) return FCP_OK;
+  const long long n8 = n / 8;  // n = Hq*T*D with D in {64, 128}
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long want = (n8 + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(want < 8LL * sms ? want : 8LL * sms);
+  dq_convert_kernel<<<grid, 256, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale);
+  FCP_CUDA_TRY(cudaGetLastError(), "dq convert launch");
+  return FCP_OK;
+}
+
+fcp_status launch_prologue(int64_t T, const void* o, const void* dout, int hq, int D, float* di, float* dq_acc,
+                           cudaStream_t s) {
+  if (T == 0) return FCP_OK;
+  const dim3 grid(static_cast<unsigned>((T + kRowWarps - 1) / kRowWarps), static_cast<unsigned>(hq));
+  const auto* po = static_cast<const __nv_bfloat16*>(o);
+  const auto* pd = static_cast<const __nv_bfloat16*>(dout);
+  if (D == 128)
+    prologue_kernel<128><<<grid, 32 * kRowWarps, 0, s>>>(po, pd, T, di, dq_acc);
+  else
+    prologue_kernel<64><<<grid, 32 * kRowWarps, 0, s>>>(po, pd, T, di, dq_acc);
+  FCP_CUDA_TRY(cudaGetLastError(), "bwd prologue launch");
+  return FCP_OK;
+}
+
+}  // namespace fcp
+
+using namespace fcp;
+
+extern "C" {
+
+fcp_status fcp_plan_upload(const fcp_plan* plan, void* d_plan, size_t bytes, void* stream) {
+  if (plan == nullptr || d_plan == nullptr) return FCP_ERR_INVALID;
+  if (!plan->distributed) return FCP_ERR_STATE;
+  if (bytes < plan->layout.total || (reinterpret_cast<uintptr_t>(d_plan) & 255u) != 0) return FCP_ERR_INVALID;
+  FCP_CUDA_TRY(cudaMemcpyAsync(d_plan, plan->image.data(), plan->layout.total, cudaMemcpyHostToDevice,
+                               static_cast<cudaStream_t>(stream)),
+               "plan upload");
+  return FCP_OK;
+}
+
+fcp_status fcp_device_error(const void* d_plan, int32_t* code, void* stream) {
+  if (d_plan == nullptr || code == nullptr) return FCP_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  FCP_CUDA_TRY(cudaMemcpyAsync(&v, d_plan, sizeof(v), cudaMemcpyDeviceToHost, s), "error word read");
+  FCP_CUDA_TRY(cudaStreamSynchronize(s), "error word sync");
+  *code = v;
+  if (v != 0) {
+    FCP_CUDA_TRY(cudaMemsetAsync(const_cast<void*>(d_plan), 0, sizeof(int32_t), s), "error word clear");
+    FCP_CUDA_TRY(cudaStreamSynchronize(s), "error word clear sync");
+    return FCP_ERR_DEVICE;
+  }
+  return FCP_OK;
+}
+
+fcp_status fcp_block_attn_merge(const fcp_plan* plan, const void* d_plan, const float* part_o, const float* part_lse,
+                                int32_t hq, int32_t head_dim, void* o, float* lse, void* stream) {
+  if (plan == nullptr || d_plan == nullptr) return FCP_ERR_INVALID;
+  if (!plan->distributed) return FCP_ERR_STATE;
+  if (hq <= 0) return FCP_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return FCP_ERR_UNSUPPORTED;
+  const int64_t T = plan->total_tokens;
+  if (T == 0) return FCP_OK;
+  if (!part_o || !part_lse || !o || !lse || !aligned16(part_o) || !aligned16(o)) return FCP_ERR_INVALID;
+  const DevLayout& L = plan->layout;
+  const dim3 grid(static_cast<unsigned>((T + kRowWarps - 1) / kRowWarps), static_cast<unsigned>(hq));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto* qsegs = dev_array<QSeg>(d_plan, L.qsegs);
+  const auto* tok2 = dev_array<int>(d_plan, L.tok2qseg);
+  const auto* runs = dev_array<fcp_run>(d_plan, L.runs);
+  auto* out = static_cast<__nv_bfloat16*>(o);
+  if (head_dim == 128)
+    merge_kernel<128><<<grid, 32 * kRowWarps, 0, s>>>(qsegs, tok2, runs, part_o, part_lse, plan->partial_rows, T,
+                                                     out, lse);
+  else
+    merge_kernel<64><<<grid, 32 * kRowWarps, 0, s>>>(qsegs, tok2, runs, part_o, part_lse, plan->partial_rows, T,
+                                                    out, lse);
+  FCP_CUDA_TRY(cudaGetLastError(), "merge launch");
+  return FCP_OK;
+}
+
+fcp_status fcp_block_attn_bwd_prologue(const fcp_plan* plan, const void* o, const void* dout, int32_t hq,
+                                       int32_t head_dim, float* di, float* dq_acc, void* stream) {
+  if (plan == nullptr || hq <= 0) return FCP_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return FCP_ERR_UNSUPPORTED;
+  if (plan->total_tokens == 0) return FCP_OK;
+  if (!o || !dout || !di || !dq_acc || !aligned16(o) || !aligned16(dout) || !aligned16(dq_acc))
+    return FCP_ERR_INVALID;
+  return launch_prologue(plan->total_tokens, o, dout, hq, head_dim, di, dq_acc, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

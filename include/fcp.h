@@ -1,0 +1,199 @@
+/*
+ * fcp.h -- C ABI of the block-wise variable-length attention library (FCP hot path).
+ *
+ * The operations follow "Unleashing Scalable Context Parallelism for Foundation
+ * Models Pre-Training via FCP" (arXiv 2605.08524):
+ *   - Section 3.3 (problem formulation): sequences S = {s_1..s_tau}, workers
+ *     W = {w_1..w_N}, a sharding function G: s_i -> {B_i1..B_ik_i} and an
+ *     assignment function M: B -> w; worker load Comp(w) = sum of f(B) over its blocks.
+ *   - Section 4.1 (block distributor): fixed-size blocks, short sequences packed into
+ *     the fewest blocks; LPT assignment to the least-loaded worker under a strict
+ *     per-worker token limit (Section 3.2, "Memory").
+ *   - Section 3.2 / Figure 4: Zig-Zag pairing of a causal sequence's blocks.
+ *   - Section 2.2: attention O = Softmax(Q K^T / sqrt(D) (+) M) V over [H, L, D]
+ *     tensors; Section 2.3: associativity, partial results over slices of L reduced
+ *     to the final output (here: the log-sum-exp merge).
+ *   - Section 4.2 (bottom-up coalescer): c consecutive block sub-stages of a worker
+ *     executed as one stage.
+ *
+ * Conventions for every call:
+ *   - Device tensors are packed over tokens in input order: Q, O, dO, dQ are
+ *     [Hq, T, D] bf16, K, V, dK, dV are [Hkv, T, D] bf16, LSE is [Hq, T] float32
+ *     (natural log), all contiguous, row-major, D innermost. T is the sum of the
+ *     sequence lengths given to fcp_partition. Base addresses must be 16-byte aligned.
+ *   - Query head h reads KV head h / (Hq / Hkv). Scale is 1/sqrt(D). D is 64 or 128.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Device calls are asynchronous on that stream and only enqueue work.
+ *   - The caller owns every device buffer. The library owns only the host plan
+ *     (released by fcp_plan_free) and allocates no device memory.
+ *   - No call asserts, traps or exits. Errors are returned as fcp_status; on
+ *     FCP_ERR_CUDA, fcp_last_error() gives the CUDA error text. A kernel that gives
+ *     up a bounded wait sets an error word in the device plan image; read it with
+ *     fcp_device_error().
+ *   - A host plan is not thread-safe; distinct plans are independent.
+ */
+#ifndef FCP_H_
+#define FCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FCP_OK = 0,
+  FCP_ERR_INVALID = 1,     /* a malformed argument (null pointer, negative length, bad shape) */
+  FCP_ERR_CAPACITY = 2,    /* a block fits no worker under the token cap */
+  FCP_ERR_UNSUPPORTED = 3, /* a valid but unsupported shape (e.g. D not in {64,128}) */
+  FCP_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  FCP_ERR_STATE = 5,       /* calls out of order (e.g. upload before distribute) */
+  FCP_ERR_DEVICE = 6       /* a kernel reported a device-side error (bounded wait gave up) */
+} fcp_status;
+
+typedef enum { FCP_MASK_FULL = 0, FCP_MASK_CAUSAL_DIAG = 1 } fcp_mask_kind;
+
+/* One block B of the sharding G. A packed block (seq = -1) holds several short
+ * sequences as consecutive segments. zz_partner is the Zig-Zag partner of block
+ * seq_block_idx in a causal sequence of seq_nblocks blocks (seq_nblocks-1-idx), or -1.
+ * cost is f(B): the unmasked (query, key) score pairs whose query lies in B. */
+typedef struct {
+  int32_t first_seg, n_segs, tokens, seq, seq_block_idx, seq_nblocks, zz_partner, worker;
+  int64_t cost;
+} fcp_block;
+
+/* A contiguous token range of one sequence inside a block; tok0 is its offset in T. */
+typedef struct {
+  int32_t seq, start_in_seq, len, tok0;
+} fcp_segment;
+
+/* A work item: the query range [q_tok0, q_tok0+q_len) against the key range
+ * [kv_tok0, kv_tok0+kv_len). FULL: every key visible. CAUSAL_DIAG: the two ranges are
+ * the same and key j is visible to query i iff j <= i. run: its partial-result slot. */
+typedef struct {
+  int32_t worker, q_block, kv_block, q_tok0, q_len, kv_tok0, kv_len, mask, run, reserved;
+} fcp_item;
+
+/* A run: items [item_begin, item_end) of one worker over one query range, reduced into
+ * one partial (O, LSE) at rows [part_row0, part_row0 + q_len) of the partial buffers. */
+typedef struct {
+  int32_t worker, q_block, q_tok0, q_len, item_begin, item_end, part_row0, reserved;
+} fcp_run;
+
+typedef struct fcp_plan fcp_plan;
+
+/* Read-only view of a host plan. Pointers stay valid until the next mutating call on
+ * the plan (fcp_distribute, fcp_coalesce) or fcp_plan_free. */
+typedef struct {
+  int32_t n_seqs, n_blocks, n_segs, n_items, n_runs, n_workers, block_size, causal, coalesce;
+  int32_t distributed;
+  int64_t total_tokens, token_cap, total_pairs, partial_rows;
+  const int32_t* seqlens;
+  const fcp_block* blocks;
+  const fcp_segment* segs;
+  const fcp_item* items;
+  const fcp_run* runs;
+  const int64_t* worker_load;   /* Comp(w): sum of block costs, n_workers entries */
+  const int64_t* worker_tokens; /* sum of len(B) per worker, n_workers entries */
+} fcp_plan_view;
+
+/* Sharding G (Section 4.1, "Sharding Policy"; Zig-Zag of Section 3.2, Figure 4).
+ * seqlens: n_seqs lengths >= 0 (host memory, copied). A sequence of length >= block_size
+ * becomes ceil(L/block_size) blocks aligned at its start (the last may be short); the
+ * shorter ones are packed first-fit-decreasing (ties: lower sequence index) into
+ * block_size-token blocks. Block ids: unpacked sequences in input order, then packed
+ * blocks. causal != 0 selects the causal mask for every sequence. On success *out
+ * receives a new plan owned by the caller (fcp_plan_free). Errors: FCP_ERR_INVALID for a
+ * null pointer, n_seqs < 0, block_size <= 0, a negative length or T >= 2^31. */
+fcp_status fcp_partition(const int32_t* seqlens, int32_t n_seqs, int32_t block_size, int32_t causal,
+                         fcp_plan** out);
+
+/* Assignment M (Section 4.1, "Assignment Policy"; token limit of Section 3.2): blocks in
+ * decreasing cost (ties: lower id) each go to the least-loaded worker (ties: lower id)
+ * whose tokens + len(B) <= token_cap; token_cap <= 0 selects block_size*ceil(K/N). Then
+ * builds the work list: per worker, per owned block (ascending id), per segment; an
+ * unpacked causal block j of a sequence pairs with KV blocks 0..j (j: CAUSAL_DIAG, others
+ * FULL), a full-mask block with every block of its sequence, a packed segment with itself.
+ * Runs are rebuilt with coalesce degree 1 (one partial per item). Errors: FCP_ERR_INVALID
+ * (null plan, n_workers <= 0), FCP_ERR_CAPACITY (the plan is left undistributed). */
+fcp_status fcp_distribute(fcp_plan* plan, int32_t n_workers, int64_t token_cap);
+
+/* Bottom-up coalescing (Section 4.2): rebuild runs so that up to `degree` consecutive
+ * items of one worker over the same query range share one partial result. degree = 1
+ * gives one partial per (Q-block, KV-block) pair. Errors: FCP_ERR_INVALID (degree <= 0),
+ * FCP_ERR_STATE (not distributed). */
+fcp_status fcp_coalesce(fcp_plan* plan, int32_t degree);
+
+/* Fill *view with read-only pointers into the plan. */
+fcp_status fcp_plan_query(const fcp_plan* plan, fcp_plan_view* view);
+
+/* Bytes of the device image of a distributed plan (work list, runs, tile schedules,
+ * token-to-range map, error word); 0 if not distributed. */
+size_t fcp_plan_device_bytes(const fcp_plan* plan);
+
+/* Copy the device image into caller-owned device memory d_plan (>= fcp_plan_device_bytes,
+ * 256-byte aligned) on `stream`, clearing its error word. The host plan must stay alive
+ * and unmodified while kernels that use d_plan run. Errors: FCP_ERR_STATE, FCP_ERR_INVALID
+ * (too small or misaligned), FCP_ERR_CUDA. */
+fcp_status fcp_plan_upload(const fcp_plan* plan, void* d_plan, size_t bytes, void* stream);
+
+/* Sizes of the partial buffers for (Hq, D): part_o float32 [Hq, partial_rows, D] and
+ * part_lse float32 [Hq, partial_rows]. */
+fcp_status fcp_partial_sizes(const fcp_plan* plan, int32_t hq, int32_t head_dim, size_t* o_bytes,
+                             size_t* lse_bytes);
+
+/* Forward over the work list (Section 2.2 attention per item; Section 2.3 partial results):
+ * for every run r, query head h and query row i of the run's range, the softmax of the
+ * scaled masked scores over the keys of the run's items, giving part_o[h, part_row0 + i, :]
+ * (normalised over those keys) and part_lse[h, part_row0 + i] (natural log-sum-exp).
+ * Inputs q, k, v bf16 device tensors as above; outputs float32 device buffers sized by
+ * fcp_partial_sizes. Errors: FCP_ERR_INVALID (nulls, Hq % Hkv != 0),
+ * FCP_ERR_UNSUPPORTED (D), FCP_ERR_STATE, FCP_ERR_CUDA. */
+fcp_status fcp_block_attn_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
+                              const void* v, int32_t hq, int32_t hkv, int32_t head_dim, float* part_o,
+                              float* part_lse, void* stream);
+
+/* Associative log-sum-exp merge (Section 2.3) of every run's partial into the final
+ * output: per (h, token) with partials s over its query range, m = max lse_s,
+ * w_s = exp(lse_s - m), o = sum w_s O_s / sum w_s (bf16), lse = m + log sum w_s (float32).
+ * o is [Hq, T, D] bf16, lse [Hq, T] float32. */
+fcp_status fcp_block_attn_merge(const fcp_plan* plan, const void* d_plan, const float* part_o,
+                                const float* part_lse, int32_t hq, int32_t head_dim, void* o, float* lse,
+                                void* stream);
+
+/* Backward prologue: di[h, t] = sum_d dO[h,t,d] * O[h,t,d] (float32 [Hq, T]) and
+ * dq_acc[h, t, :] = 0 (float32 [Hq, T, D]). */
+fcp_status fcp_block_attn_bwd_prologue(const fcp_plan* plan, const void* o, const void* dout, int32_t hq,
+                                       int32_t head_dim, float* di, float* dq_acc, void* stream);
+
+/* Workspace bytes for fcp_block_attn_bwd: a float32 dQ accumulator [Hq, T, D] followed by
+ * the float32 Di [Hq, T] (each 256-byte aligned). */
+size_t fcp_bwd_workspace_bytes(const fcp_plan* plan, int32_t hq, int32_t head_dim);
+
+/* Backward over the same work list (the exact gradient of the Section 2.2 attention; the
+ * pages implement a backward but describe only the forward): with P = exp(S*scale - lse),
+ * dV = sum P^T dO, dP = dO V^T, dS = P * (dP - Di), dQ = scale dS K, dK = scale dS^T Q,
+ * KV gradients summed over the query heads of their group. lse is the merged LSE from
+ * fcp_block_attn_merge, o the merged output. Launches the prologue, the tile kernel and
+ * the dQ conversion on `stream`. dq [Hq,T,D], dk and dv [Hkv,T,D] bf16 outputs; workspace
+ * of fcp_bwd_workspace_bytes, 256-byte aligned. */
+fcp_status fcp_block_attn_bwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
+                              const void* v, const void* o, const void* dout, const float* lse, int32_t hq,
+                              int32_t hkv, int32_t head_dim, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, copy the device plan's error word to *code (0 = none; else the
+ * kernel and wait that gave up) and clear it. Returns FCP_ERR_DEVICE if it was set. */
+fcp_status fcp_device_error(const void* d_plan, int32_t* code, void* stream);
+
+void fcp_plan_free(fcp_plan* plan);
+const char* fcp_status_string(fcp_status status);
+/* Detail of the last FCP_ERR_CUDA in this thread ("" if none). */
+const char* fcp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FCP_H_ */

@@ -159,24 +159,28 @@ def attention_dq_rows(q_rows, do_rows, k_seq, v_seq, rows: Iterable[int], causal
 
 
 def attention_dkv_rows(q_seq, do_seq, k_seq, v_seq, kv_rows: Iterable[int], causal: bool,
-                       scale: Optional[float] = None) -> Tuple[np.ndarray, np.ndarray]:
+                       scale: Optional[float] = None, q_offset: int = 0) -> Tuple[np.ndarray, np.ndarray]:
     """dK, dV [n, D] for selected key rows of one sequence, one KV group.
 
-    q_seq, do_seq: [G, L, D] all query heads of the group over the whole sequence;
-    k_seq, v_seq: [L, D]. Under a causal mask only query rows i >= min(kv_rows)
-    contribute, so key rows near the end of a long sequence are cheap.
+    q_seq, do_seq: [G, m, D] all query heads of the group for the query positions
+    q_offset .. q_offset+m-1, which must run to the end of the sequence and include every
+    query that sees a selected key (causal: every position >= min(kv_rows); full mask:
+    all); k_seq, v_seq: [L, D] the whole sequence. Key rows near the end of a long causal
+    sequence therefore need only a short tail of queries.
     """
     q_seq, do_seq = _as64(q_seq), _as64(do_seq)
     k_seq, v_seq = _as64(k_seq), _as64(v_seq)
     kv_rows = np.asarray(list(kv_rows), dtype=np.int64)
-    G, L, D = q_seq.shape
+    G, m, D = q_seq.shape
+    L = k_seq.shape[0]
+    assert q_offset + m == L, "query rows must run to the end of the sequence"
+    assert q_offset <= (int(kv_rows.min()) if causal else 0), "missing query rows that see the keys"
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    first = int(kv_rows.min()) if causal else 0
     dk = np.zeros((len(kv_rows), D))
     dv = np.zeros((len(kv_rows), D))
-    for r0 in range(first, L, _ROW_CHUNK):
-        r1 = min(L, r0 + _ROW_CHUNK)
-        rows = np.arange(r0, r1)
+    for r0 in range(0, m, _ROW_CHUNK):
+        r1 = min(m, r0 + _ROW_CHUNK)
+        rows = np.arange(q_offset + r0, q_offset + r1)
         p, _ = _softmax_rows(_scores(q_seq[:, r0:r1], k_seq, rows, causal, scale))
         dO = do_seq[:, r0:r1]
         o_rows = np.einsum("gnl,ld->gnd", p, v_seq)

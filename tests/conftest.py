@@ -26,3 +26,15 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def fcp():
+    """The package with libfcp.so built (compiles for sm_103a if the sources changed)."""
+    from context_parallelism_fcp_gb300 import _build
+
+    _build.build()
+    import context_parallelism_fcp_gb300 as pkg
+
+    pkg.lib()
+    return pkg

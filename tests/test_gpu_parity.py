@@ -1,0 +1,164 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small batches are compared element by element (all heads, all tokens, all outputs); the
+full-size workloads, in the launch configuration the benchmark times, on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as A
+from oracle import plan as P
+from tests import parity_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _sync():
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("w", W.small_cases(), ids=lambda w: w.name)
+def test_forward_and_backward_small(fcp, w):
+    r = U.run_path(fcp, w)
+    ro, rl = A.attention_forward(r["q"], r["k"], r["v"], w.seqlens, w.causal)
+    U.check_forward(U.np64(r["o"]), U.np64(r["lse"]), ro, rl, w.name)
+    rdq, rdk, rdv = A.attention_backward(r["q"], r["k"], r["v"], r["do"], w.seqlens, w.causal)
+    for name, got, ref in zip(("dq", "dk", "dv"), r["grads"], (rdq, rdk, rdv)):
+        U.check_grad(name, U.np64(got), ref, w.name)
+
+
+@pytest.mark.parametrize("c", [1, 2, 16])
+def test_coalesce_degree_does_not_change_the_result(fcp, c):
+    w = W.Workload("mixed small", [1500, 40, 700, 2600], 512, 8, 2, 128, 3, True)
+    r = U.run_path(fcp, w, coalesce=c)
+    ro, rl = A.attention_forward(r["q"], r["k"], r["v"], w.seqlens, w.causal)
+    U.check_forward(U.np64(r["o"]), U.np64(r["lse"]), ro, rl, f"c={c}")
+
+
+def _merge_expected(w, part_o, part_lse, coalesce):
+    """Oracle merge of the partial buffers, using the oracle plan's runs (bit-identical to the
+    library's plan, which the CPU tests pin)."""
+    part = P.partition(w.seqlens, w.block_size, w.causal)
+    dist = P.distribute(part, w.n_workers, w.token_cap)
+    runs = P.coalesce(dist["items"], coalesce)
+    T = w.total_tokens
+    po = part_o.double().cpu().numpy()
+    pl = part_lse.double().cpu().numpy()
+    o = np.zeros((w.hq, T, w.head_dim))
+    lse = np.full((w.hq, T), -np.inf)
+    by_range = {}
+    for rn in runs:
+        by_range.setdefault((rn[2], rn[3]), []).append(rn[6])
+    for (tok0, qlen), row0s in by_range.items():
+        rows = np.array(row0s)[:, None] + np.arange(qlen)[None, :]  # [S, qlen]
+        mo, ml = A.lse_merge(np.moveaxis(po[:, rows], 1, 0), np.moveaxis(pl[:, rows], 1, 0))
+        o[:, tok0:tok0 + qlen] = mo
+        lse[:, tok0:tok0 + qlen] = ml
+    return o, lse
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("neg_inf", [0.0, 0.3])
+def test_merge_kernel_matches_oracle_merge(fcp, head_dim, neg_inf):
+    w = W.Workload("merge", [1000, 300, 2049, 17], 256, 4, 2, head_dim, 3, True)
+    coalesce = 2
+    att = fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, w.hq, w.hkv, w.head_dim,
+                           coalesce=coalesce, backward=False)
+    rows = att.part_o.shape[1]
+    o_p, l_p = W.make_partials(1, w.hq, rows, head_dim, seed=3, device="cuda", neg_inf_frac=neg_inf)
+    att.part_o.copy_(o_p[0])
+    att.part_lse.copy_(l_p[0])
+    o = torch.empty((w.hq, w.total_tokens, head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.hq, w.total_tokens), dtype=torch.float32, device="cuda")
+    fcp.block_attn_merge(att.plan, att.d_plan, att.part_o, att.part_lse, o, lse)
+    torch.cuda.synchronize()
+    eo, el = _merge_expected(w, att.part_o, att.part_lse, coalesce)
+    got = U.np64(o)
+    # bf16 output rounding: |err| <= 2^-8 |x| (+ float32 accumulation)
+    assert np.all(np.abs(got - eo) <= 2.0 ** -8 * np.abs(eo) + 1e-5)
+    gl = U.np64(lse)
+    fin = np.isfinite(el)
+    assert np.array_equal(np.isfinite(gl), fin)
+    assert np.abs(gl[fin] - el[fin]).max() <= 1e-5 * max(1.0, np.abs(el[fin]).max())
+    assert np.all(got[:, ~fin.all(axis=0)][~np.isfinite(el[:, ~fin.all(axis=0)])] == 0)
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_bwd_prologue_matches_oracle(fcp, head_dim):
+    w = W.Workload("prologue", [777, 64], 256, 4, 2, head_dim, 2, True)
+    plan = fcp.Plan(w.seqlens, w.block_size, w.causal).distribute(2)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    o = torch.randn((4, w.total_tokens, head_dim), generator=g, device="cuda").to(torch.bfloat16)
+    do = torch.randn((4, w.total_tokens, head_dim), generator=g, device="cuda").to(torch.bfloat16)
+    di = torch.empty((4, w.total_tokens), dtype=torch.float32, device="cuda")
+    acc = torch.full((4, w.total_tokens, head_dim), 7.0, dtype=torch.float32, device="cuda")
+    fcp.block_attn_bwd_prologue(plan, o, do, di, acc)
+    torch.cuda.synchronize()
+    ref = A.rowsum_do_o(do, o)
+    assert np.abs(U.np64(di) - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
+    assert torch.count_nonzero(acc).item() == 0
+
+
+def test_edge_cases(fcp):
+    # one token, lengths at and around the block size, packed singles, both masks
+    for seqlens, b, causal in (([1], 128, True), ([128, 129, 127], 128, True), ([1, 1, 1, 1], 2, False),
+                               ([256], 128, False), ([3, 700], 256, True)):
+        w = W.Workload("edge", seqlens, b, 4, 2, 64, 2, causal)
+        r = U.run_path(fcp, w)
+        ro, rl = A.attention_forward(r["q"], r["k"], r["v"], w.seqlens, w.causal)
+        U.check_forward(U.np64(r["o"]), U.np64(r["lse"]), ro, rl, str(seqlens))
+        rdq, rdk, rdv = A.attention_backward(r["q"], r["k"], r["v"], r["do"], w.seqlens, w.causal)
+        for name, got, ref in zip(("dq", "dk", "dv"), r["grads"], (rdq, rdk, rdv)):
+            U.check_grad(name, U.np64(got), ref, str(seqlens))
+
+
+def test_empty_batch_is_a_no_op(fcp):
+    att = fcp.FcpAttention([0, 0], 64, True, 2, 4, 2, 64)
+    q = torch.empty((4, 0, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((2, 0, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = att.forward(q, k, k)
+    dq, dk, dv = att.backward(q, k, k, o, lse, q)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and dq.numel() == 0
+    att.check_device_error()
+
+
+# ------------------------------------------------------------------ full-size workloads
+def test_full_mask_sampled(fcp):
+    w = W.full_mask()
+    r = U.run_path(fcp, w)
+    U.sampled_forward(r, w, rows_per_seq=24)
+
+
+def test_causal_mixed_sampled(fcp):
+    w = W.causal_mixed()
+    r = U.run_path(fcp, w)
+    U.sampled_forward(r, w, rows_per_seq=32)
+    U.sampled_backward(r, w, rows_per_seq=16, kv_tail=48)
+
+
+@pytest.mark.parametrize("b", [512, 4096])
+def test_block_sweep_sampled(fcp, b):
+    w = W.block_sweep(b)
+    r = U.run_path(fcp, w)
+    U.sampled_forward(r, w, rows_per_seq=64)
+    U.sampled_backward(r, w, rows_per_seq=16, kv_tail=32)
+
+
+def test_long_causal_sampled(fcp):
+    """524288-token sequence: 256 seeded query rows per KV-head group (all 8 heads of the group),
+    dQ on 32 of them, dK/dV on the last 32 key rows, plus the merge invariant: merging at
+    coalesce degree 16 gives the same output as degree 64 (one partial per query block)."""
+    w = W.long_causal()
+    r = U.run_path(fcp, w)
+    U.sampled_forward(r, w, rows_per_seq=256)
+    U.sampled_backward(r, w, rows_per_seq=32, kv_tail=32)
+    o16 = r["o"].clone()
+    del r
+    torch.cuda.empty_cache()
+    r64 = U.run_path(fcp, w, coalesce=64, backward=False)
+    assert (r64["o"].float() - o16.float()).abs().max().item() <= 2e-2

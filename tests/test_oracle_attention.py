@@ -208,6 +208,12 @@ def test_row_helpers_agree_with_whole_sequence():
                                             kv_rows, causal)
             assert np.abs(rdk - dk[g, a + np.array(kv_rows)]).max() < 1e-12
             assert np.abs(rdv - dv[g, a + np.array(kv_rows)]).max() < 1e-12
+            if causal:  # only the query tail from the first selected key is needed
+                tail = [69, 60, 55]
+                rdk, rdv = A.attention_dkv_rows(q[hs, a + 55:a + L], do[hs, a + 55:a + L], k[g, a:a + L],
+                                                v[g, a:a + L], tail, causal, q_offset=55)
+                assert np.abs(rdk - dk[g, a + np.array(tail)]).max() < 1e-12
+                assert np.abs(rdv - dv[g, a + np.array(tail)]).max() < 1e-12
 
 
 def test_di_identity():
