@@ -29,6 +29,8 @@ __all__ = [
     "block_attn_merge",
     "block_attn_bwd",
     "block_attn_bwd_prologue",
+    "block_attn_bwd_tiles",
+    "block_attn_bwd_dq_convert",
     "FcpAttention",
     "MASK_FULL",
     "MASK_CAUSAL_DIAG",
@@ -109,6 +111,8 @@ _SIGNATURES = {
     "fcp_block_attn_bwd_prologue": (_ST, [_P, _P, _P, _I32, _I32, _P, _P, _P]),
     "fcp_bwd_workspace_bytes": (_SZ, [_P, _I32, _I32]),
     "fcp_block_attn_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "fcp_block_attn_bwd_tiles": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "fcp_block_attn_bwd_dq_convert": (_ST, [_P, _P, _I32, _I32, _P, _P]),
     "fcp_device_error": (_ST, [_P, ctypes.POINTER(_I32), _P]),
     "fcp_plan_free": (None, [_P]),
     "fcp_status_string": (ctypes.c_char_p, [_ST]),
@@ -307,6 +311,30 @@ def block_attn_bwd(plan: Plan, d_plan, q, k, v, o, dout, lse, dq, dk, dv, worksp
                                     _ptr(lse), hq, hkv, D, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "fcp_block_attn_bwd")
+
+
+def block_attn_bwd_tiles(plan: Plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, stream=None) -> None:
+    """The backward tile kernel alone (fcp_block_attn_bwd_tiles); dq_acc/di from the prologue."""
+    import torch
+
+    hq, T, D = q.shape
+    hkv = k.shape[0]
+    _need(dq_acc, torch.float32, (hq, T, D), "dq_acc")
+    _need(di, torch.float32, (hq, T), "di")
+    _check(lib().fcp_block_attn_bwd_tiles(plan.handle, _ptr(d_plan), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                          _ptr(lse), _ptr(di), hq, hkv, D, _ptr(dq_acc), _ptr(dk), _ptr(dv),
+                                          _stream(stream)), "fcp_block_attn_bwd_tiles")
+
+
+def block_attn_bwd_dq_convert(plan: Plan, dq_acc, dq, stream=None) -> None:
+    """dq = bf16(dq_acc / sqrt(D)) (fcp_block_attn_bwd_dq_convert)."""
+    import torch
+
+    hq, T, D = dq.shape
+    _need(dq_acc, torch.float32, (hq, T, D), "dq_acc")
+    _need(dq, torch.bfloat16, (hq, T, D), "dq")
+    _check(lib().fcp_block_attn_bwd_dq_convert(plan.handle, _ptr(dq_acc), hq, D, _ptr(dq), _stream(stream)),
+           "fcp_block_attn_bwd_dq_convert")
 
 
 def device_error(d_plan, stream=None) -> int:

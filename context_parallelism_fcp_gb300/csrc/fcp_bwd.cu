@@ -443,6 +443,43 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 using namespace fcp;
 
+namespace {
+fcp_status check_common(const fcp_plan* plan, const void* d_plan, int32_t hq, int32_t hkv, int32_t head_dim) {
+  if (plan == nullptr || d_plan == nullptr) return FCP_ERR_INVALID;
+  if (!plan->distributed) return FCP_ERR_STATE;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return FCP_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return FCP_ERR_UNSUPPORTED;
+  return FCP_OK;
+}
+}  // namespace
+
+extern "C" fcp_status fcp_block_attn_bwd_tiles(const fcp_plan* plan, const void* d_plan, const void* q,
+                                               const void* k, const void* v, const void* dout, const float* lse,
+                                               const float* di, int32_t hq, int32_t hkv, int32_t head_dim,
+                                               float* dq_acc, void* dk, void* dv, void* stream) {
+  fcp_status st = check_common(plan, d_plan, hq, hkv, head_dim);
+  if (st != FCP_OK) return st;
+  if (plan->total_tokens == 0) return FCP_OK;
+  if (!q || !k || !v || !dout || !lse || !di || !dq_acc || !dk || !dv) return FCP_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(dq_acc))
+    return FCP_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (head_dim == 128) return launch_bwd<128>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, s);
+  return launch_bwd<64>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, s);
+}
+
+extern "C" fcp_status fcp_block_attn_bwd_dq_convert(const fcp_plan* plan, const float* dq_acc, int32_t hq,
+                                                    int32_t head_dim, void* dq, void* stream) {
+  if (plan == nullptr || hq <= 0) return FCP_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return FCP_ERR_UNSUPPORTED;
+  if (plan->total_tokens == 0) return FCP_OK;
+  if (!dq_acc || !dq || !aligned16(dq_acc) || !aligned16(dq)) return FCP_ERR_INVALID;
+  return launch_dq_convert(dq_acc, dq, static_cast<long long>(hq) * plan->total_tokens * head_dim,
+                           static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim))),
+                           static_cast<cudaStream_t>(stream));
+}
+
 extern "C" fcp_status fcp_block_attn_bwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
                                          const void* v, const void* o, const void* dout, const float* lse,
                                          int32_t hq, int32_t hkv, int32_t head_dim, void* dq, void* dk, void* dv,

@@ -183,6 +183,18 @@ fcp_status fcp_block_attn_bwd(const fcp_plan* plan, const void* d_plan, const vo
                               int32_t hkv, int32_t head_dim, void* dq, void* dk, void* dv, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* The tile kernel of fcp_block_attn_bwd alone: given di and a dq_acc zeroed by the prologue,
+ * accumulates float32 dQ / scale into dq_acc [Hq, T, D] (atomically) and writes dk, dv
+ * [Hkv, T, D] bf16. dq_acc is caller-owned scratch (256-byte aligned). */
+fcp_status fcp_block_attn_bwd_tiles(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
+                                    const void* v, const void* dout, const float* lse, const float* di,
+                                    int32_t hq, int32_t hkv, int32_t head_dim, float* dq_acc, void* dk, void* dv,
+                                    void* stream);
+
+/* The last step of fcp_block_attn_bwd alone: dq = bf16(dq_acc / sqrt(D)) over [Hq, T, D]. */
+fcp_status fcp_block_attn_bwd_dq_convert(const fcp_plan* plan, const float* dq_acc, int32_t hq, int32_t head_dim,
+                                         void* dq, void* stream);
+
 /* Synchronise `stream`, copy the device plan's error word to *code (0 = none; else the
  * kernel and wait that gave up) and clear it. Returns FCP_ERR_DEVICE if it was set. */
 fcp_status fcp_device_error(const void* d_plan, int32_t* code, void* stream);

@@ -5,7 +5,9 @@ Tolerances. Forward (fixed by the target): O max-abs <= 2e-2 and mean-abs <= 2e-
 the oracle, LSE max-abs <= 1e-3. Backward (derived from bf16 arithmetic): the kernels round
 P and dS to bf16 (unit roundoff u = 2^-8) before the gradient MMAs and the outputs to bf16,
 so each gradient element carries a relative error of a few u; the tests require
-max-abs <= 5e-2 * max(1, max|ref|) and mean-abs <= 1e-2 * mean|ref| (about 2.5 u) per tensor.
+max-abs <= 5e-2 * max(1, max|ref|) and mean-abs <= 1e-2 * mean|ref| + 1e-5 (about 2.5 u,
+with an absolute floor for gradients that cancel to exactly zero, e.g. dQ of a one-token
+sequence, where the kernel returns rounding noise of order u * |dP|) per tensor.
 """
 from __future__ import annotations
 
@@ -16,7 +18,7 @@ import workloads as W
 from oracle import attention as A
 
 O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
-G_MAX_REL, G_MEAN_REL = 5e-2, 1e-2
+G_MAX_REL, G_MEAN_REL, G_MEAN_ABS = 5e-2, 1e-2, 1e-5
 
 
 def run_path(fcp, w: W.Workload, coalesce=None, backward=None, device="cuda"):
@@ -47,7 +49,7 @@ def check_forward(o, lse, ro, rl, where=""):
 def check_grad(name, got, ref, where=""):
     e = np.abs(got - ref)
     assert e.max() <= G_MAX_REL * max(1.0, np.abs(ref).max()), f"{where} {name} max {e.max():.3e}"
-    assert e.mean() <= G_MEAN_REL * np.abs(ref).mean(), \
+    assert e.mean() <= G_MEAN_REL * np.abs(ref).mean() + G_MEAN_ABS, \
         f"{where} {name} mean {e.mean():.3e} vs mean|ref| {np.abs(ref).mean():.3e}"
 
 
