@@ -66,6 +66,23 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Maximum of a per-rank number over the process group (the identity on one process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Units all ranks processed divided by the slowest rank's step time."""
+    return flops_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def flops_of(seqlens, causal, hq, d):
     pairs = sum(L * (L + 1) // 2 if causal else L * L for L in seqlens)
     fwd = 4.0 * hq * d * pairs
@@ -303,14 +320,8 @@ def bench_fcp(args):
 
     ms = statistics.mean(t["total"] for t in times)
     phase = {k: statistics.mean(t[k] for t in times) for k in ("fwd", "merge", "prologue", "bwd", "convert")}
-    if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    total_flops = (step.fwd_flops + step.bwd_flops) * world
-    value = total_flops / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(ms, dev)
+    value = whole_job_tflops(step.fwd_flops + step.bwd_flops, world, ms)
     sustained = pk["bf16_tflops_sustained"]
     fwd_tf = step.fwd_flops / (phase["fwd"] * 1e-3) / 1e12
     bwd_tf = step.bwd_flops / (phase["bwd"] * 1e-3) / 1e12
