@@ -113,6 +113,8 @@ _SIGNATURES = {
     "fcp_block_attn_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "fcp_block_attn_bwd_tiles": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "fcp_block_attn_bwd_dq_convert": (_ST, [_P, _P, _I32, _I32, _P, _P]),
+    "fcp_bwd_static_scratch_bytes": (_SZ, []),
+    "fcp_block_attn_bwd_static_scratch": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "fcp_device_error": (_ST, [_P, ctypes.POINTER(_I32), _P]),
     "fcp_plan_free": (None, [_P]),
     "fcp_status_string": (ctypes.c_char_p, [_ST]),

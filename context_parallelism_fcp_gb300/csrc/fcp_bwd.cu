@@ -20,6 +20,9 @@
 // Per step the MMAs run S^T, dP^T | dV += P^T dO, dK += dS^T Q, dQ = dS K, all issued by
 // one thread in that order, so each MMA that overwrites TMEM columns follows the MMA that
 // last read them.
+#include <mutex>
+#include <string>
+
 #include "fcp_cuda_util.h"
 #include "fcp_sm100.cuh"
 
@@ -508,4 +511,67 @@ extern "C" fcp_status fcp_block_attn_bwd(const fcp_plan* plan, const void* d_pla
   if (st != FCP_OK) return st;
   return launch_dq_convert(dq_acc, dq, static_cast<long long>(hq) * T * head_dim,
                            static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim))), s);
+}
+
+// ---------------------------------------------------------------------------------------
+// Backward without any allocation by the caller or the library.
+//
+// Some callers cannot call cudaMalloc at all: code that runs inside a memory pool or
+// arena that owns every byte of the device (a framework that pre-reserved the GPU), code
+// on a path where allocating would synchronise the device or break an allocation-free
+// contract (real-time or inference-serving loops), or plain C hosts without a device
+// allocator of their own. For them the backward's scratch (the float32 dQ accumulator and
+// Di) lives in a fixed array in device memory that this library owns. Every GPU that
+// loads the library holds this array until the process exits.
+namespace fcp {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) uint8_t g_bwd_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_bwd_scratch on the current device. The host-side name of the array
+// is only a stand-in, so the address is looked up once per device (with that device
+// current) and cached.
+fcp_status static_scratch(void** out) {
+  int dev = 0;
+  FCP_CUDA_TRY(cudaGetDevice(&dev), "static scratch: current device");
+  if (dev < 0 || dev >= kMaxDevices) return FCP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    FCP_CUDA_TRY(cudaGetSymbolAddress(&p, g_bwd_scratch), "static scratch: cudaGetSymbolAddress");
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return FCP_OK;
+}
+
+}  // namespace
+}  // namespace fcp
+
+extern "C" size_t fcp_bwd_static_scratch_bytes(void) { return fcp::kStaticScratchBytes; }
+
+extern "C" fcp_status fcp_block_attn_bwd_static_scratch(const fcp_plan* plan, const void* d_plan, const void* q,
+                                                        const void* k, const void* v, const void* o,
+                                                        const void* dout, const float* lse, int32_t hq,
+                                                        int32_t hkv, int32_t head_dim, void* dq, void* dk, void* dv,
+                                                        void* stream) {
+  if (plan == nullptr || hq <= 0 || head_dim <= 0) return FCP_ERR_INVALID;
+  const size_t need = fcp_bwd_workspace_bytes(plan, hq, head_dim);
+  if (need > fcp::kStaticScratchBytes) {
+    fcp::set_last_error("backward scratch of " + std::to_string(need) + " bytes exceeds the library's static " +
+                        std::to_string(fcp::kStaticScratchBytes) + "-byte array; use fcp_block_attn_bwd");
+    return FCP_ERR_UNSUPPORTED;
+  }
+  void* scratch = nullptr;
+  fcp_status st = fcp::static_scratch(&scratch);
+  if (st != FCP_OK) return st;
+  // The prologue rewrites the whole dQ accumulator with zeros and Di in full on every call,
+  // so what the previous call left in the array does not matter.
+  return fcp_block_attn_bwd(plan, d_plan, q, k, v, o, dout, lse, hq, hkv, head_dim, dq, dk, dv, scratch,
+                            fcp::kStaticScratchBytes, stream);
 }

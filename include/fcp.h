@@ -195,6 +195,24 @@ fcp_status fcp_block_attn_bwd_tiles(const fcp_plan* plan, const void* d_plan, co
 fcp_status fcp_block_attn_bwd_dq_convert(const fcp_plan* plan, const float* dq_acc, int32_t hq, int32_t head_dim,
                                          void* dq, void* stream);
 
+/* Backward that allocates nothing (the paper has no counterpart; this serves callers that
+ * cannot call cudaMalloc -- code running inside a memory pool that owns the whole device, an
+ * allocation-free serving or real-time loop, or a C host without a device allocator). Same
+ * arguments, results and errors as fcp_block_attn_bwd, without the workspace: the scratch
+ * (float32 dQ accumulator and Di, fcp_bwd_workspace_bytes) lives in a fixed device array
+ * of fcp_bwd_static_scratch_bytes() = 32 MiB inside the library, which every GPU that loads
+ * the library holds until the process exits. A larger requirement returns
+ * FCP_ERR_UNSUPPORTED with the sizes in fcp_last_error(). The first call on a device looks
+ * up the array's device address with that device current; make that first call before any
+ * stream capture. All calls share the one array: calls whose work overlaps on the GPU (other
+ * streams, other threads) race on it and must be serialised by the caller. Each call
+ * re-zeroes the accumulator itself, so nothing needs clearing between calls. */
+size_t fcp_bwd_static_scratch_bytes(void);
+fcp_status fcp_block_attn_bwd_static_scratch(const fcp_plan* plan, const void* d_plan, const void* q,
+                                             const void* k, const void* v, const void* o, const void* dout,
+                                             const float* lse, int32_t hq, int32_t hkv, int32_t head_dim, void* dq,
+                                             void* dk, void* dv, void* stream);
+
 /* Synchronise `stream`, copy the device plan's error word to *code (0 = none; else the
  * kernel and wait that gave up) and clear it. Returns FCP_ERR_DEVICE if it was set. */
 fcp_status fcp_device_error(const void* d_plan, int32_t* code, void* stream);
