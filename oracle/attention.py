@@ -43,7 +43,7 @@ def cu_seqlens_of(seqlens: Sequence[int]) -> np.ndarray:
 def _scores(qh: np.ndarray, kg: np.ndarray, rows: np.ndarray, causal: bool, scale: float) -> np.ndarray:
     """Scaled scores of query rows `rows` (positions in the sequence) against every key of the
     sequence, with the causal mask as -inf. qh: [G, n, D] queries of those rows; kg: [L, D]."""
-    s = np.einsum("gnd,ld->gnl", qh, kg) * scale
+    s = np.matmul(qh, kg.T) * scale
     if causal:
         keys = np.arange(kg.shape[0])
         s = np.where(keys[None, None, :] > rows[None, :, None], -np.inf, s)
@@ -84,7 +84,7 @@ def attention_forward(q, k, v, seqlens: Sequence[int], causal: bool,
                 r1 = min(b, r0 + _ROW_CHUNK)
                 rows = np.arange(r0 - a, r1 - a)
                 p, l_ = _softmax_rows(_scores(q[hs, r0:r1], kg, rows, causal, scale))
-                o[hs, r0:r1] = np.einsum("gnl,ld->gnd", p, vg)
+                o[hs, r0:r1] = np.matmul(p, vg)
                 lse[hs, r0:r1] = l_
     return o, lse
 
@@ -116,13 +116,13 @@ def attention_backward(q, k, v, do, seqlens: Sequence[int], causal: bool,
                 rows = np.arange(r0 - a, r1 - a)
                 p, _ = _softmax_rows(_scores(q[hs, r0:r1], kg, rows, causal, scale))
                 dO = do[hs, r0:r1]
-                o_rows = np.einsum("gnl,ld->gnd", p, vg)
+                o_rows = np.matmul(p, vg)
                 di = np.sum(dO * o_rows, axis=-1)
-                dp = np.einsum("gnd,ld->gnl", dO, vg)
+                dp = np.matmul(dO, vg.T)
                 ds = p * (dp - di[..., None])
-                dv[g, a:b] += np.einsum("gnl,gnd->ld", p, dO)
-                dq[hs, r0:r1] = scale * np.einsum("gnl,ld->gnd", ds, kg)
-                dk[g, a:b] += scale * np.einsum("gnl,gnd->ld", ds, q[hs, r0:r1])
+                dv[g, a:b] += np.matmul(p.transpose(0, 2, 1), dO).sum(axis=0)
+                dq[hs, r0:r1] = scale * np.matmul(ds, kg)
+                dk[g, a:b] += scale * np.matmul(ds.transpose(0, 2, 1), q[hs, r0:r1]).sum(axis=0)
     return dq, dk, dv
 
 
@@ -139,7 +139,7 @@ def attention_rows(q_rows, k_seq, v_seq, rows: Iterable[int], causal: bool,
     D = q_rows.shape[-1]
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     p, lse = _softmax_rows(_scores(q_rows, k_seq, rows, causal, scale))
-    return np.einsum("gnl,ld->gnd", p, v_seq), lse
+    return np.matmul(p, v_seq), lse
 
 
 def attention_dq_rows(q_rows, do_rows, k_seq, v_seq, rows: Iterable[int], causal: bool,
@@ -151,11 +151,11 @@ def attention_dq_rows(q_rows, do_rows, k_seq, v_seq, rows: Iterable[int], causal
     D = q_rows.shape[-1]
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     p, _ = _softmax_rows(_scores(q_rows, k_seq, rows, causal, scale))
-    o_rows = np.einsum("gnl,ld->gnd", p, v_seq)
+    o_rows = np.matmul(p, v_seq)
     di = np.sum(do_rows * o_rows, axis=-1)
-    dp = np.einsum("gnd,ld->gnl", do_rows, v_seq)
+    dp = np.matmul(do_rows, v_seq.T)
     ds = p * (dp - di[..., None])
-    return scale * np.einsum("gnl,ld->gnd", ds, k_seq)
+    return scale * np.matmul(ds, k_seq)
 
 
 def attention_dkv_rows(q_seq, do_seq, k_seq, v_seq, kv_rows: Iterable[int], causal: bool,
@@ -183,13 +183,13 @@ def attention_dkv_rows(q_seq, do_seq, k_seq, v_seq, kv_rows: Iterable[int], caus
         rows = np.arange(q_offset + r0, q_offset + r1)
         p, _ = _softmax_rows(_scores(q_seq[:, r0:r1], k_seq, rows, causal, scale))
         dO = do_seq[:, r0:r1]
-        o_rows = np.einsum("gnl,ld->gnd", p, v_seq)
+        o_rows = np.matmul(p, v_seq)
         di = np.sum(dO * o_rows, axis=-1)
         psel = p[:, :, kv_rows]  # [G, n_q, n_kv]
-        dp = np.einsum("gnd,md->gnm", dO, v_seq[kv_rows])
+        dp = np.matmul(dO, v_seq[kv_rows].T)
         ds = psel * (dp - di[..., None])
-        dv += np.einsum("gnm,gnd->md", psel, dO)
-        dk += scale * np.einsum("gnm,gnd->md", ds, q_seq[:, r0:r1])
+        dv += np.matmul(psel.transpose(0, 2, 1), dO).sum(axis=0)
+        dk += scale * np.matmul(ds.transpose(0, 2, 1), q_seq[:, r0:r1]).sum(axis=0)
     return dk, dv
 
 
