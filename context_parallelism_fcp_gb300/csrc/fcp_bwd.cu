@@ -31,6 +31,9 @@ namespace fcp {
 fcp_status launch_prologue(int64_t T, const void* o, const void* dout, int hq, int D, float* di, float* dq_acc,
                            cudaStream_t s);
 fcp_status launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale, cudaStream_t s);
+fcp_status launch_bwd_d128(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
+                           const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
+                           int hq, int hkv, cudaStream_t stream);
 
 namespace {
 
@@ -403,6 +406,10 @@ template <int D>
 fcp_status launch_bwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
                       const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
                       int hq, int hkv, cudaStream_t stream) {
+  if constexpr (D == 128) {
+    // head_dim 128 runs the pipelined kernel with 64-row query steps
+    return launch_bwd_d128(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, stream);
+  } else {
   using C = BwdCfg<D>;
   const DevLayout& L = plan->layout;
   if (L.n_bwd_units == 0) return FCP_OK;
@@ -437,6 +444,7 @@ fcp_status launch_bwd(const fcp_plan* plan, const void* d_plan, const void* q, c
   bwd_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
   FCP_CUDA_TRY(cudaGetLastError(), "bwd launch");
   return FCP_OK;
+  }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

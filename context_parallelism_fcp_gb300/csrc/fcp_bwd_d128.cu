@@ -1,0 +1,461 @@
+// Backward block attention for head_dim 128 on sm_103a: a pipelined tile kernel.
+//
+// Same mathematics and work decomposition as the generic backward kernel (the exact gradient
+// of the attention of "Unleashing Scalable Context Parallelism for Foundation Models
+// Pre-Training via FCP", Section 2.2, over the reversed work list): one CTA owns a 128-row
+// key tile of one key range and one KV head, and walks every (query head of the group, item
+// reading this key range, query step) accumulating dK and dV in TMEM.
+//
+// What differs is the schedule. A query step is 64 rows, so the S^T/dP^T accumulators of a
+// step need 128 TMEM columns and two steps fit beside dV and dK:
+//   columns [128b, 128b+64)     S^T of buffer b (b = step & 1); later P^T (bf16, 32 cols);
+//                               later dQ^T = K^T dS^T (128 lanes = channels x 64 queries)
+//   columns [128b+64, 128b+128) dP^T of buffer b; later dS^T (bf16, 32 cols)
+//   columns [256, 384) dV, [384, 512) dK
+// The MMA warp issues S^T/dP^T of step i+1 before it waits for the gradient warps of step
+// i, so the tensor core works on the next step while the current one is turned into P and
+// dS. dQ^T is computed with the channels on TMEM lanes, so the drain warps add it to the
+// float32 accumulator with one coalesced 128-byte atomic line per warp instruction, and free
+// the TMEM buffer as soon as the values are in registers.
+// Warps: 0-7 gradient (two warpgroups, 32 query columns each; thread = key row = TMEM lane),
+// 8-11 dQ drain (thread = channel = TMEM lane), 12 TMA producer (Q/dO/LSE/Di, 3 stages),
+// 13 TMEM allocator and single-thread MMA issuer.
+#include "fcp_cuda_util.h"
+#include "fcp_sm100.cuh"
+
+namespace fcp {
+namespace {
+
+using namespace dev;
+
+constexpr int kD = 128;
+constexpr int kBN = 128;  // key rows per CTA
+constexpr int kBQ = 64;   // query rows per step
+constexpr int kStages = 3;
+constexpr int kThreads = 448;
+
+constexpr int kKVTile = kBN * kD * 2;      // 32768: 2 panels of [128 rows][64 ch]
+constexpr int kKVPanel = kBN * 128;        // 16384
+constexpr int kQTile = kBQ * kD * 2;       // 16384: 2 panels of [64 rows][64 ch]
+constexpr int kQPanel = kBQ * 128;         // 8192
+constexpr int kDSTile = kBN * kBQ * 2;     // 16384: [128 kv rows][64 q] bf16, one panel
+
+constexpr int kOffK = 0;
+constexpr int kOffV = kKVTile;
+constexpr int kOffQ = 2 * kKVTile;                          // kStages tiles
+constexpr int kOffDO = kOffQ + kStages * kQTile;            // kStages tiles
+constexpr int kOffDS = kOffDO + kStages * kQTile;           // 2 buffers
+constexpr int kOffVec = kOffDS + 2 * kDSTile;               // kStages x (lse2[64], di[64])
+constexpr int kOffBar = kOffVec + kStages * 2 * kBQ * 4;
+constexpr int kSmemBytes = kOffBar + 256;
+
+enum : int {
+  B_KVFULL = 0,
+  B_QFULL = 1,     // kStages
+  B_QEMPTY = 4,    // kStages
+  B_STFULL = 7,    // 2 buffers
+  B_DSFULL = 9,    // 2 buffers
+  B_DSEMPTY = 11,  // 2 buffers
+  B_DQFULL = 13,   // 2 buffers
+  B_DQEMPTY = 15,  // 2 buffers
+  B_ACCDONE = 17,
+  B_RDONE = 18,    // 2 buffers: both gradient warpgroups have read S^T/dP^T
+  B_COUNT = 20
+};
+static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+static_assert(kSmemBytes <= 232448, "shared memory per block");
+
+// S^T, dP^T: M = 128 keys, N = 64 queries, both operands K-major.
+constexpr uint32_t kIdescST = idesc_bf16(kBN, kBQ, false, false);
+// dV, dK: M = 128 keys, N = 128 channels, A from TMEM, B (dO / Q) MN-major.
+constexpr uint32_t kIdescAcc = idesc_bf16(kBN, kD, false, true);
+// dQ^T = K^T dS^T: M = 128 channels, N = 64 queries, A (K read transposed) and B MN-major.
+constexpr uint32_t kIdescDQ = idesc_bf16(kD, kBQ, true, true);
+
+struct Args {
+  const fcp_item* items;
+  const KvSeg* kvsegs;
+  const int* kv_items;
+  const BwdUnit* units;
+  const float* lse;
+  const float* di;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  long long T;
+  int hkv, group;
+  float scale_log2, scale;
+  int* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_d128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const Args a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, kErrSmemAlign);
+    return;
+  }
+  const uint32_t sb = smem_u32(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + B_COUNT * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + B_COUNT * 8 + 4);
+  float* vec = reinterpret_cast<float*>(smem + kOffVec);  // [stage][lse2[64] | di[64]]
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int unit_idx = blockIdx.x / a.hkv;
+  const int kvh = blockIdx.x - unit_idx * a.hkv;
+  const BwdUnit unit = a.units[unit_idx];
+  const KvSeg seg = a.kvsegs[unit.kvseg];
+  const int kt = unit.kv_tile;
+  const int kv_row0 = seg.tok0 + kt * kBN;
+  const int kv_valid = seg.len - kt * kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_KVFULL), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_QFULL + s), 32);
+      mbar_init(bar(B_QEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_STFULL + b), 1);
+      mbar_init(bar(B_DSFULL + b), 256);
+      mbar_init(bar(B_DSEMPTY + b), 1);
+      mbar_init(bar(B_DQFULL + b), 1);
+      mbar_init(bar(B_DQEMPTY + b), 128);
+      mbar_init(bar(B_RDONE + b), 256);
+    }
+    mbar_init(bar(B_ACCDONE), 1);
+    *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
+    mbar_fence_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = *abort_flag != 0;
+
+  // Steps: for each query head of the group, each item whose key range is this one, each
+  // 64-row query step that sees this key tile (a causal diagonal item starts at the step
+  // holding the tile's first key). body(step, h, item, qs) returns false to stop.
+  auto for_each_step = [&](auto&& body) -> int {
+    int step = 0;
+    for (int hh = 0; hh < a.group; ++hh) {
+      const int h = kvh * a.group + hh;
+      for (int li = seg.list_begin; li < seg.list_end; ++li) {
+        const fcp_item itm = a.items[a.kv_items[li]];
+        const int q_end = (itm.q_len + kBQ - 1) / kBQ;
+        const int q_first = itm.mask == FCP_MASK_CAUSAL_DIAG ? (kt * kBN) / kBQ : 0;
+        for (int qs = q_first; qs < q_end; ++qs, ++step)
+          if (!body(step, h, itm, qs)) return step;
+      }
+    }
+    return step;
+  };
+
+  int n_steps = 0;
+  if (warp == 12) {
+    // ---------------------------------------------------------------- producer
+    bool ok = !skip;
+    if (ok && lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(bar(B_KVFULL), 2 * kKVTile);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        tma_load_3d(sb + kOffK + p * kKVPanel, &tmK, bar(B_KVFULL), p * 64, kv_row0, kvh);
+        tma_load_3d(sb + kOffV + p * kKVPanel, &tmV, bar(B_KVFULL), p * 64, kv_row0, kvh);
+      }
+    }
+    if (ok) {
+      n_steps = for_each_step([&](const int step, const int h, const fcp_item& itm, const int qs) -> bool {
+        const int s = step % kStages;
+        const uint32_t ph = (step / kStages) & 1;
+        ok = mbar_wait(bar(B_QEMPTY + s), ph ^ 1, abort_flag, a.err, kErrBwdWait + 1);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        const int qrow0 = itm.q_tok0 + qs * kBQ;
+        const int q_valid = itm.q_len - qs * kBQ;
+        if (lane == 0) {
+          mbar_expect_tx(bar(B_QFULL + s), 2 * kQTile);
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            tma_load_3d(sb + kOffQ + s * kQTile + p * kQPanel, &tmQ, bar(B_QFULL + s), p * 64, qrow0, h);
+            tma_load_3d(sb + kOffDO + s * kQTile + p * kQPanel, &tmDO, bar(B_QFULL + s), p * 64, qrow0, h);
+          }
+        }
+        // LSE in log2 units and Di of the step's query rows; rows past the range get
+        // LSE = +inf (P = 0) and Di = 0
+        float* v = vec + s * 2 * kBQ;
+        const long long rowbase = static_cast<long long>(h) * a.T + qrow0;
+#pragma unroll
+        for (int i = 0; i < kBQ / 32; ++i) {
+          const int c = i * 32 + lane;
+          const bool in = c < q_valid;
+          v[c] = in ? a.lse[rowbase + c] * 1.4426950408889634f : INFINITY;
+          v[kBQ + c] = in ? a.di[rowbase + c] : 0.f;
+        }
+        mbar_arrive(bar(B_QFULL + s));
+        return true;
+      });
+    }
+  } else if (warp == 13) {
+    // ---------------------------------------------------------------- MMA issuer
+    bool ok = !skip;
+    if (lane == 0) {
+      if (ok) ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, a.err, kErrBwdWait + 2);
+      tc_fence_after();
+      const uint32_t t_dv = tmem + 256, t_dk = tmem + 384;
+      // number of steps, walked once without waiting
+      const int total = ok ? for_each_step([](int, int, const fcp_item&, int) { return true; }) : 0;
+      auto issue_sdp = [&](int j) -> bool {
+        const int s = j % kStages, b = j & 1;
+        if (!mbar_wait(bar(B_QFULL + s), (j / kStages) & 1, abort_flag, a.err, kErrBwdWait + 3)) return false;
+        // buffer b is free once the dQ^T of step j-2 has been read out of it
+        if (!mbar_wait(bar(B_DQEMPTY + b), ((j >> 1) & 1) ^ 1, abort_flag, a.err, kErrBwdWait + 4)) return false;
+        tc_fence_after();
+        const uint32_t qb = sb + kOffQ + s * kQTile, db = sb + kOffDO + s * kQTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * kKVPanel + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * kQPanel + (kk & 3) * 32;
+          mma_ss(tmem + 128 * b, sdesc_sw128(sb + kOffK + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), kIdescST,
+                 kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * kKVPanel + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * kQPanel + (kk & 3) * 32;
+          mma_ss(tmem + 128 * b + 64, sdesc_sw128(sb + kOffV + ko, 16, 1024), sdesc_sw128(db + qo, 16, 1024),
+                 kIdescST, kk > 0);
+        }
+        tc_commit(bar(B_STFULL + b));
+        return true;
+      };
+      if (ok && total > 0) ok = issue_sdp(0);
+      for (int i = 0; i < total && ok; ++i) {
+        if (i + 1 < total) {
+          ok = issue_sdp(i + 1);
+          if (!ok) break;
+        }
+        const int s = i % kStages, b = i & 1;
+        ok = mbar_wait(bar(B_DSFULL + b), (i >> 1) & 1, abort_flag, a.err, kErrBwdWait + 5);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qb = sb + kOffQ + s * kQTile, db = sb + kOffDO + s * kQTile;
+        // dV += P^T dO and dK += dS^T Q: K = 64 queries in 4 steps of 16 (8 TMEM columns)
+#pragma unroll
+        for (int kk = 0; kk < kBQ / 16; ++kk)
+          mma_ts(t_dv, tmem + 128 * b + kk * 8, sdesc_sw128(db + kk * 2048, kQPanel, 1024), kIdescAcc,
+                 (i > 0 || kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < kBQ / 16; ++kk)
+          mma_ts(t_dk, tmem + 128 * b + 64 + kk * 8, sdesc_sw128(qb + kk * 2048, kQPanel, 1024), kIdescAcc,
+                 (i > 0 || kk > 0));
+        // dQ^T = K^T dS^T: K = 128 keys in 8 steps of 16 rows (2048 bytes)
+        const uint32_t dsb = sb + kOffDS + b * kDSTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ss(tmem + 128 * b, sdesc_sw128(sb + kOffK + kk * 2048, kKVPanel, 1024),
+                 sdesc_sw128(dsb + kk * 2048, kKVPanel, 1024), kIdescDQ, kk > 0);
+        tc_commit(bar(B_DQFULL + b));
+        tc_commit(bar(B_DSEMPTY + b));
+        tc_commit(bar(B_QEMPTY + s));
+      }
+      n_steps = total;
+      tc_commit(bar(B_ACCDONE));
+    }
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- gradient warps
+    bool ok = !skip;
+    const int wg = warp >> 2;              // query columns [32 wg, 32 wg + 32) of a step
+    const int r = (warp & 3) * 32 + lane;  // key row = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    uint8_t* ds_row = smem + kOffDS + r * 128;
+    if (ok) {
+      n_steps = for_each_step([&](const int step, const int h, const fcp_item& itm, const int qs) -> bool {
+        const int s = step % kStages, b = step & 1;
+        // visible query columns of this key row: c >= r + (key-tile start - step start) on a
+        // causal diagonal item; none past the key range
+        int qmin = 0;
+        if (r >= kv_valid) {
+          qmin = kBQ;
+        } else if (itm.mask == FCP_MASK_CAUSAL_DIAG) {
+          qmin = max(0, r + kt * kBN - qs * kBQ);
+        }
+        ok = mbar_wait(bar(B_QFULL + s), (step / kStages) & 1, abort_flag, a.err, kErrBwdWait + 7);
+        if (ok) ok = mbar_wait(bar(B_STFULL + b), (step >> 1) & 1, abort_flag, a.err, kErrBwdWait + 8);
+        // the dS^T tile of buffer b is free once the dQ^T MMA of step-2 has read it
+        if (ok) ok = mbar_wait(bar(B_DSEMPTY + b), ((step >> 1) & 1) ^ 1, abort_flag, a.err, kErrBwdWait + 9);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        tc_fence_after();
+        const float* lse2 = vec + s * 2 * kBQ;
+        const float* dis = lse2 + kBQ;
+        uint32_t sv[32], dv[32];
+        tmem_ld32(lane_base + 128 * b + 32 * wg, sv);
+        tmem_ld32(lane_base + 128 * b + 64 + 32 * wg, dv);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 32 * wg + 2 * e;
+          float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
+          if (c0 >= qmin) {
+            p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * e]), a.scale_log2, -lse2[c0]));
+            d0 = p0 * (__uint_as_float(dv[2 * e]) - dis[c0]);
+          }
+          if (c0 + 1 >= qmin) {
+            p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), a.scale_log2, -lse2[c0 + 1]));
+            d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - dis[c0 + 1]);
+          }
+          pp[e] = pack_bf16(p0, p1);
+          dd[e] = pack_bf16(d0, d1);
+        }
+        // both warpgroups have read their S^T/dP^T columns before either overwrites
+        // columns the other reads (a bounded mbarrier wait, not a named barrier, so that a
+        // warp that gave up cannot leave the others waiting)
+        tc_fence_before();
+        mbar_arrive(bar(B_RDONE + b));
+        ok = mbar_wait(bar(B_RDONE + b), (step >> 1) & 1, abort_flag, a.err, kErrBwdWait + 12);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        tc_fence_after();
+        tmem_st16(lane_base + 128 * b + 16 * wg, pp);
+        tmem_st16(lane_base + 128 * b + 64 + 16 * wg, dd);
+        // dS^T row r, queries [32 wg, 32 wg + 32): 16-byte chunks 4 wg .. 4 wg + 3 of the
+        // 128-byte row, 128-byte swizzle (chunk XOR row & 7)
+        uint8_t* drow = ds_row + b * kDSTile;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int chunk = (4 * wg + x) ^ (r & 7);
+          *reinterpret_cast<uint4*>(drow + chunk * 16) = make_uint4(dd[4 * x], dd[4 * x + 1], dd[4 * x + 2], dd[4 * x + 3]);
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(B_DSFULL + b));
+        return true;
+      });
+    }
+    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK (bf16)
+    if (ok) ok = mbar_wait(bar(B_ACCDONE), 0, abort_flag, a.err, kErrBwdWait + 10);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const bool store = r < kv_valid;
+      const long long row = static_cast<long long>(kvh) * a.T + kv_row0 + r;
+      __nv_bfloat16* dst = (wg == 0 ? a.dv : a.dk) + row * kD;
+      const float f = wg == 0 ? 1.f : a.scale;
+      const uint32_t base = lane_base + (wg == 0 ? 256 : 384);
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t x[32];
+        if (n_steps > 0) {
+          tmem_ld32(base + c * 32, x);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = 0u;
+        }
+        if (store) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 pk;
+            pk.x = pack_bf16(__uint_as_float(x[8 * e + 0]) * f, __uint_as_float(x[8 * e + 1]) * f);
+            pk.y = pack_bf16(__uint_as_float(x[8 * e + 2]) * f, __uint_as_float(x[8 * e + 3]) * f);
+            pk.z = pack_bf16(__uint_as_float(x[8 * e + 4]) * f, __uint_as_float(x[8 * e + 5]) * f);
+            pk.w = pack_bf16(__uint_as_float(x[8 * e + 6]) * f, __uint_as_float(x[8 * e + 7]) * f);
+            reinterpret_cast<uint4*>(dst + c * 32)[e] = pk;
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ drain (warps 8-11)
+    bool ok = !skip;
+    const int d = (warp & 3) * 32 + lane;  // channel = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    if (ok) {
+      n_steps = for_each_step([&](const int step, const int h, const fcp_item& itm, const int qs) -> bool {
+        const int b = step & 1;
+        ok = mbar_wait(bar(B_DQFULL + b), (step >> 1) & 1, abort_flag, a.err, kErrBwdWait + 11);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        tc_fence_after();
+        uint32_t x0[32], x1[32];
+        tmem_ld32(lane_base + 128 * b, x0);
+        tmem_ld32(lane_base + 128 * b + 32, x1);
+        tc_fence_before();
+        mbar_arrive(bar(B_DQEMPTY + b));  // TMEM buffer free; the adds run from registers
+        const int q_valid = min(kBQ, itm.q_len - qs * kBQ);
+        float* dst = a.dq_acc + (static_cast<long long>(h) * a.T + itm.q_tok0 + qs * kBQ) * kD + d;
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          if (q < q_valid) atomicAdd(dst + static_cast<long long>(q) * kD, __uint_as_float(x0[q]));
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          if (32 + q < q_valid) atomicAdd(dst + static_cast<long long>(32 + q) * kD, __uint_as_float(x1[q]));
+        return true;
+      });
+    }
+  }
+
+  if (*abort_flag) {
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 1000000ull) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+// Launch of the head_dim-128 backward tile kernel (same contract as fcp_block_attn_bwd_tiles).
+fcp_status launch_bwd_d128(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
+                           const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
+                           int hq, int hkv, cudaStream_t stream) {
+  const DevLayout& L = plan->layout;
+  if (L.n_bwd_units == 0) return FCP_OK;
+  const int64_t T = plan->total_tokens;
+  CUtensorMap mq, mk, mv, mdo;
+  fcp_status st;
+  if ((st = make_bf16_map(&mq, q, hq, T, kD, kBQ)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mk, k, hkv, T, kD, kBN)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mv, v, hkv, T, kD, kBN)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mdo, dout, hq, T, kD, kBQ)) != FCP_OK) return st;
+  Args a;
+  a.items = dev_array<fcp_item>(d_plan, L.items);
+  a.kvsegs = dev_array<KvSeg>(d_plan, L.kvsegs);
+  a.kv_items = dev_array<int>(d_plan, L.kv_items);
+  a.units = dev_array<BwdUnit>(d_plan, L.bwd_units);
+  a.lse = lse;
+  a.di = di;
+  a.dq_acc = dq_acc;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.T = T;
+  a.hkv = hkv;
+  a.group = hq / hkv;
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+  a.err = dev_error_word(d_plan);
+  FCP_CUDA_TRY(cudaFuncSetAttribute(bwd_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
+               "bwd d128 smem attribute");
+  const long long grid = static_cast<long long>(L.n_bwd_units) * hkv;
+  if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
+  bwd_d128_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  FCP_CUDA_TRY(cudaGetLastError(), "bwd d128 launch");
+  return FCP_OK;
+}
+
+}  // namespace fcp
