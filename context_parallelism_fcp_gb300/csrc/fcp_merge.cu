@@ -51,47 +51,45 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// grid (ceil(T / kRowWarps), Hq); warp w of block x handles token x*kRowWarps + w of head y.
+constexpr int kMergeRows = 4;  // consecutive tokens per warp
+
+template <int N>
+__device__ __forceinline__ void store_bf16(__nv_bfloat16* dst, const float (&x)[N], float inv) {
+  if constexpr (N == 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x[0] * inv, x[1] * inv);
+    __nv_bfloat162 b = __floats2bfloat162_rn(x[2] * inv, x[3] * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&a);
+    pk.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(x[0] * inv, x[1] * inv);
+  }
+}
+
+// One row merged by the whole warp: partials at rows off + k * stride (k < nr), walked 32 at
+// a time. Used when the warp's rows have more partials than the unrolled path holds.
 template <int D>
-__global__ void __launch_bounds__(32 * kRowWarps)
-    merge_kernel(const QSeg* __restrict__ qsegs, const int* __restrict__ tok2qseg, const fcp_run* __restrict__ runs,
-                 const float* __restrict__ part_o, const float* __restrict__ part_lse, long long part_rows,
-                 long long T, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+__device__ __forceinline__ void merge_row_general(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                                                  long long off, int stride, int nr, int lane, float (&acc)[D / 32],
+                                                  float& m_out, float& wsum_out) {
   using V = Vec<D>;
   constexpr int N = V::N;
-  const int lane = threadIdx.x & 31;
-  const long long t = static_cast<long long>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const int h = blockIdx.y;
-  const QSeg qs = qsegs[tok2qseg[t]];
-  const int row = static_cast<int>(t - qs.tok0);
-  const long long head_base = static_cast<long long>(h) * part_rows + row;
-  const int nr = qs.run_end - qs.run_begin;
-
-  // max of the partial LSEs, lanes striding over runs
   float m = -INFINITY;
-  for (int i = lane; i < nr; i += 32) m = fmaxf(m, __ldg(part_lse + head_base + runs[qs.run_begin + i].part_row0));
+  for (int i = lane; i < nr; i += 32) m = fmaxf(m, __ldg(part_lse + off + static_cast<long long>(i) * stride));
   m = warp_max(m);
-
-  float acc[N];
 #pragma unroll
   for (int e = 0; e < N; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (m != -INFINITY) {
     for (int base = 0; base < nr; base += 32) {
-      // each lane fetches one run's weight and row offset, then the warp walks them
       float w_l = 0.f;
-      long long off_l = 0;
-      if (base + lane < nr) {
-        const long long pr = head_base + runs[qs.run_begin + base + lane].part_row0;
-        w_l = __expf(__ldg(part_lse + pr) - m);
-        off_l = pr;
-      }
+      if (base + lane < nr) w_l = __expf(__ldg(part_lse + off + static_cast<long long>(base + lane) * stride) - m);
       const int cnt = min(32, nr - base);
 #pragma unroll 4
       for (int i = 0; i < cnt; ++i) {
         const float w = __shfl_sync(0xffffffffu, w_l, i);
-        const long long pr = __shfl_sync(0xffffffffu, off_l, i);
+        const long long pr = off + static_cast<long long>(base + i) * stride;
         float x[N];
         vload(reinterpret_cast<const typename V::F*>(part_o + pr * D) + lane, x);
 #pragma unroll
@@ -100,19 +98,118 @@ __global__ void __launch_bounds__(32 * kRowWarps)
       }
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = o + (static_cast<long long>(h) * T + t) * D + lane * N;
-  if constexpr (N == 4) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&a);
-    pk.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(dst) = pk;
-  } else {
-    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+  m_out = m;
+  wsum_out = wsum;
+}
+
+constexpr int kMergePairs = 8;  // (row, partial) pairs a warp fetches at once
+
+// grid (ceil(T / (kRowWarps * kMergeRows)), Hq): warp w of block x merges tokens
+// [(x*kRowWarps + w) * kMergeRows, +kMergeRows) of head y. Each token's partial rows come
+// from one 16-byte record (base, stride, count), so the partial rows of all the warp's
+// (row, partial) pairs are loaded at once, independently of their LSEs.
+template <int D>
+__global__ void __launch_bounds__(32 * kRowWarps)
+    merge_kernel(const TokPart* __restrict__ tok2part, const float* __restrict__ part_o,
+                 const float* __restrict__ part_lse, long long part_rows, long long T, __nv_bfloat16* __restrict__ o,
+                 float* __restrict__ lse) {
+  using V = Vec<D>;
+  constexpr int N = V::N;
+  constexpr int R = kMergeRows;
+  const int lane = threadIdx.x & 31;
+  const long long t0 = (static_cast<long long>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5)) * R;
+  if (t0 >= T) return;
+  const long long hoff = static_cast<long long>(blockIdx.y) * part_rows;
+
+  int4 info = make_int4(0, 0, 0, 0);
+  if (lane < R && t0 + lane < T) info = __ldg(reinterpret_cast<const int4*>(tok2part + t0 + lane));
+  int nr[R], stride[R], start[R + 1];
+  long long off[R];
+  start[0] = 0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    off[i] = hoff + __shfl_sync(0xffffffffu, info.x, i);
+    stride[i] = __shfl_sync(0xffffffffu, info.y, i);
+    nr[i] = __shfl_sync(0xffffffffu, info.z, i);
+    start[i + 1] = start[i] + nr[i];
   }
-  if (lane == 0) lse[static_cast<long long>(h) * T + t] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+  const int P = start[R];
+
+  float acc[R][N];
+  float m[R], ws[R];
+  if (P <= kMergePairs) {
+    // pair p = (row i, partial k): lane p knows its row and partial-row index
+    int myrow = -1;
+    long long prow = 0;
+    if (lane < P) {
+      int i = 0;
+#pragma unroll
+      for (int j = 1; j < R; ++j)
+        if (lane >= start[j]) i = j;
+      long long oi = off[0];
+      int si = stride[0], sti = start[0];
+#pragma unroll
+      for (int j = 1; j < R; ++j)
+        if (i == j) {
+          oi = off[j];
+          si = stride[j];
+          sti = start[j];
+        }
+      myrow = i;
+      prow = oi + static_cast<long long>(lane - sti) * si;
+    }
+    // all partial rows in flight first, then the LSEs
+    float x[kMergePairs][N];
+    int rowof[kMergePairs];
+#pragma unroll
+    for (int p = 0; p < kMergePairs; ++p) {
+      const long long pr = __shfl_sync(0xffffffffu, prow, p);
+      rowof[p] = __shfl_sync(0xffffffffu, myrow, p);
+      if (p < P) {
+        vload(reinterpret_cast<const typename V::F*>(part_o + pr * D) + lane, x[p]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e) x[p][e] = 0.f;
+      }
+    }
+    const float l = lane < P ? __ldg(part_lse + prow) : -INFINITY;
+    float mine_m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      m[i] = warp_max(myrow == i ? l : -INFINITY);
+      if (myrow == i) mine_m = m[i];
+    }
+    const float w = (myrow >= 0 && l != -INFINITY) ? __expf(l - mine_m) : 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      ws[i] = warp_sum(myrow == i ? w : 0.f);
+#pragma unroll
+      for (int e = 0; e < N; ++e) acc[i][e] = 0.f;
+    }
+#pragma unroll
+    for (int p = 0; p < kMergePairs; ++p) {
+      const float wp = __shfl_sync(0xffffffffu, w, p);
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const float wi = (rowof[p] == i) ? wp : 0.f;
+#pragma unroll
+        for (int e = 0; e < N; ++e) acc[i][e] = fmaf(wi, x[p][e], acc[i][e]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < R; ++i) merge_row_general<D>(part_o, part_lse, off[i], stride[i], nr[i], lane, acc[i], m[i], ws[i]);
+  }
+
+  const long long obase = static_cast<long long>(blockIdx.y) * T;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const long long t = t0 + i;
+    if (t >= T) break;
+    const float inv = ws[i] > 0.f ? 1.f / ws[i] : 0.f;
+    store_bf16<N>(o + (obase + t) * D + lane * N, acc[i], inv);
+    if (lane == i) lse[obase + t] = ws[i] > 0.f ? m[i] + logf(ws[i]) : -INFINITY;
+  }
 }
 
 // Di[h,t] = sum_d dO*O and dq_acc[h,t,:] = 0. grid (ceil(T / kRowWarps), Hq).
@@ -237,18 +334,15 @@ fcp_status fcp_block_attn_merge(const fcp_plan* plan, const void* d_plan, const 
   if (T == 0) return FCP_OK;
   if (!part_o || !part_lse || !o || !lse || !aligned16(part_o) || !aligned16(o)) return FCP_ERR_INVALID;
   const DevLayout& L = plan->layout;
-  const dim3 grid(static_cast<unsigned>((T + kRowWarps - 1) / kRowWarps), static_cast<unsigned>(hq));
+  const long long rows_per_block = static_cast<long long>(kRowWarps) * kMergeRows;
+  const dim3 grid(static_cast<unsigned>((T + rows_per_block - 1) / rows_per_block), static_cast<unsigned>(hq));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const auto* qsegs = dev_array<QSeg>(d_plan, L.qsegs);
-  const auto* tok2 = dev_array<int>(d_plan, L.tok2qseg);
-  const auto* runs = dev_array<fcp_run>(d_plan, L.runs);
+  const auto* tok2 = dev_array<TokPart>(d_plan, L.tok2part);
   auto* out = static_cast<__nv_bfloat16*>(o);
   if (head_dim == 128)
-    merge_kernel<128><<<grid, 32 * kRowWarps, 0, s>>>(qsegs, tok2, runs, part_o, part_lse, plan->partial_rows, T,
-                                                     out, lse);
+    merge_kernel<128><<<grid, 32 * kRowWarps, 0, s>>>(tok2, part_o, part_lse, plan->partial_rows, T, out, lse);
   else
-    merge_kernel<64><<<grid, 32 * kRowWarps, 0, s>>>(qsegs, tok2, runs, part_o, part_lse, plan->partial_rows, T,
-                                                    out, lse);
+    merge_kernel<64><<<grid, 32 * kRowWarps, 0, s>>>(tok2, part_o, part_lse, plan->partial_rows, T, out, lse);
   FCP_CUDA_TRY(cudaGetLastError(), "merge launch");
   return FCP_OK;
 }

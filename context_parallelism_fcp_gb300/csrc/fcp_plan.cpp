@@ -78,7 +78,7 @@ void put(std::vector<uint8_t>& img, size_t off, const std::vector<T>& v) {
   if (!v.empty()) std::memcpy(img.data() + off, v.data(), v.size() * sizeof(T));
 }
 
-// Device image: header, items, runs, query ranges with their runs, token -> query range,
+// Device image: header, items, runs, query ranges with their runs, token -> partial rows,
 // forward units (longest first), key ranges with their items, backward units (longest first).
 bool build_image(fcp_plan* p) {
   std::vector<QSeg> qsegs;
@@ -91,10 +91,14 @@ bool build_image(fcp_plan* p) {
     }
   }
   int32_t max_runs = 0;
-  std::vector<int32_t> tok2qseg(static_cast<size_t>(p->total_tokens), -1);
-  for (int32_t s = 0; s < static_cast<int32_t>(qsegs.size()); ++s) {
-    max_runs = std::max(max_runs, qsegs[s].run_end - qsegs[s].run_begin);
-    for (int32_t t = 0; t < qsegs[s].len; ++t) tok2qseg[static_cast<size_t>(qsegs[s].tok0) + t] = s;
+  std::vector<TokPart> tok2part(static_cast<size_t>(p->total_tokens), TokPart{0, 0, 0, 0});
+  for (const QSeg& q : qsegs) {
+    max_runs = std::max(max_runs, q.run_end - q.run_begin);
+    const int32_t base = p->runs[q.run_begin].part_row0;
+    for (int32_t r = q.run_begin; r < q.run_end; ++r)
+      if (p->runs[r].part_row0 != base + (r - q.run_begin) * q.len) return false;  // rows must be contiguous
+    for (int32_t t = 0; t < q.len; ++t)
+      tok2part[static_cast<size_t>(q.tok0) + t] = TokPart{base + t, q.len, q.run_end - q.run_begin, 0};
   }
 
   // forward units with their key-tile counts; longest first, ties in run/tile order
@@ -161,8 +165,8 @@ bool build_image(fcp_plan* p) {
   off = align256(off + p->runs.size() * sizeof(fcp_run));
   L.qsegs = off;
   off = align256(off + qsegs.size() * sizeof(QSeg));
-  L.tok2qseg = off;
-  off = align256(off + tok2qseg.size() * sizeof(int32_t));
+  L.tok2part = off;
+  off = align256(off + tok2part.size() * sizeof(TokPart));
   L.fwd_units = off;
   off = align256(off + fwd_units.size() * sizeof(FwdUnit));
   L.kvsegs = off;
@@ -179,13 +183,13 @@ bool build_image(fcp_plan* p) {
   L.n_bwd_units = static_cast<int32_t>(bwd_units.size());
   L.max_runs_per_qseg = max_runs;
 
-  for (int32_t s : tok2qseg)
-    if (s < 0) return false;  // every token must belong to exactly one query range
+  for (const TokPart& tp : tok2part)
+    if (tp.count <= 0) return false;  // every token must belong to exactly one query range
   p->image.assign(L.total, 0);
   put(p->image, L.items, p->items);
   put(p->image, L.runs, p->runs);
   put(p->image, L.qsegs, qsegs);
-  put(p->image, L.tok2qseg, tok2qseg);
+  put(p->image, L.tok2part, tok2part);
   put(p->image, L.fwd_units, fwd_units);
   put(p->image, L.kvsegs, kvsegs);
   put(p->image, L.kv_items, kv_items);

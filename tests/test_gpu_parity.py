@@ -63,9 +63,12 @@ def _merge_expected(w, part_o, part_lse, coalesce):
 
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("neg_inf", [0.0, 0.3])
-def test_merge_kernel_matches_oracle_merge(fcp, head_dim, neg_inf):
-    w = W.Workload("merge", [1000, 300, 2049, 17], 256, 4, 2, head_dim, 3, True)
-    coalesce = 2
+@pytest.mark.parametrize("seqlens,coalesce", [([1000, 300, 2049, 17], 2), ([2304, 40, 3], 1)],
+                         ids=["few partials", "many partials"])
+def test_merge_kernel_matches_oracle_merge(fcp, head_dim, neg_inf, seqlens, coalesce):
+    """Partials of up to 9 runs per row: the second case puts 36 partials on the 4 rows one
+    warp merges, which takes the kernel's general path."""
+    w = W.Workload("merge", seqlens, 256, 4, 2, head_dim, 3, True)
     att = fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, w.hq, w.hkv, w.head_dim,
                            coalesce=coalesce, backward=False)
     rows = att.part_o.shape[1]
