@@ -8,10 +8,15 @@
 //
 // What differs is the schedule. A query step is 64 rows, so the S^T/dP^T accumulators of a
 // step need 128 TMEM columns and two steps fit beside dV and dK:
-//   columns [128b, 128b+64)     S^T of buffer b (b = step & 1); later P^T (bf16, 32 cols);
-//                               later dQ^T = K^T dS^T (128 lanes = channels x 64 queries)
-//   columns [128b+64, 128b+128) dP^T of buffer b; later dS^T (bf16, 32 cols)
+//   columns [128b, 128b+64)     S^T of buffer b (b = step & 1); P^T (bf16) overwrites
+//                               [128b+16, 128b+48)
+//   columns [128b+64, 128b+128) dP^T; dS^T (bf16) overwrites [128b+80, 128b+112); later
+//                               dQ^T = K^T dS^T (128 lanes = channels x 64 queries)
 //   columns [256, 384) dV, [384, 512) dK
+// Each gradient warpgroup reads 32 columns of S^T and of dP^T and writes its packed half of
+// P^T and dS^T inside the columns it has itself just read, so the two warpgroups never
+// need to wait for each other. S^T of step i+2 may be issued before the drain of step i
+// has read dQ^T (they occupy different halves of the buffer); only dP^T waits for it.
 // The MMA warp issues S^T/dP^T of step i+1 before it waits for the gradient warps of step
 // i, so the tensor core works on the next step while the current one is turned into P and
 // dS. dQ^T is computed with the channels on TMEM lanes, so the drain warps add it to the
@@ -49,20 +54,21 @@ constexpr int kOffVec = kOffDS + 2 * kDSTile;               // kStages x (lse2[6
 constexpr int kOffBar = kOffVec + kStages * 2 * kBQ * 4;
 constexpr int kSmemBytes = kOffBar + 256;
 
+// mbarrier indices, laid out from the stage count so that no two ever share a slot
 enum : int {
   B_KVFULL = 0,
-  B_QFULL = 1,     // kStages
-  B_QEMPTY = 4,    // kStages
-  B_STFULL = 7,    // 2 buffers
-  B_DSFULL = 9,    // 2 buffers
-  B_DSEMPTY = 11,  // 2 buffers
-  B_DQFULL = 13,   // 2 buffers
-  B_DQEMPTY = 15,  // 2 buffers
-  B_ACCDONE = 17,
-  B_RDONE = 18,    // 2 buffers: both gradient warpgroups have read S^T/dP^T
-  B_COUNT = 20
+  B_QFULL = 1,                     // kStages
+  B_QEMPTY = B_QFULL + kStages,    // kStages
+  B_STFULL = B_QEMPTY + kStages,   // 2 buffers
+  B_DSFULL = B_STFULL + 2,         // 2 buffers
+  B_DSEMPTY = B_DSFULL + 2,        // 2 buffers
+  B_DQFULL = B_DSEMPTY + 2,        // 2 buffers
+  B_DQEMPTY = B_DQFULL + 2,        // 2 buffers
+  B_ACCDONE = B_DQEMPTY + 2,
+  B_COUNT = B_ACCDONE + 1
 };
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+static_assert(kOffVec + kStages * 2 * kBQ * 4 == kOffBar, "vector area");
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // S^T, dP^T: M = 128 keys, N = 64 queries, both operands K-major.
@@ -124,7 +130,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_DSEMPTY + b), 1);
       mbar_init(bar(B_DQFULL + b), 1);
       mbar_init(bar(B_DQEMPTY + b), 128);
-      mbar_init(bar(B_RDONE + b), 256);
     }
     mbar_init(bar(B_ACCDONE), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
@@ -218,8 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_sdp = [&](int j) -> bool {
         const int s = j % kStages, b = j & 1;
         if (!mbar_wait(bar(B_QFULL + s), (j / kStages) & 1, abort_flag, a.err, kErrBwdWait + 3)) return false;
-        // buffer b is free once the dQ^T of step j-2 has been read out of it
-        if (!mbar_wait(bar(B_DQEMPTY + b), ((j >> 1) & 1) ^ 1, abort_flag, a.err, kErrBwdWait + 4)) return false;
         tc_fence_after();
         const uint32_t qb = sb + kOffQ + s * kQTile, db = sb + kOffDO + s * kQTile;
 #pragma unroll
@@ -229,6 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + 128 * b, sdesc_sw128(sb + kOffK + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), kIdescST,
                  kk > 0);
         }
+        // the dP^T half of buffer b is free once the dQ^T of step j-2 has been read out of it
+        if (!mbar_wait(bar(B_DQEMPTY + b), ((j >> 1) & 1) ^ 1, abort_flag, a.err, kErrBwdWait + 4)) return false;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * kKVPanel + (kk & 3) * 32;
@@ -253,17 +259,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dV += P^T dO and dK += dS^T Q: K = 64 queries in 4 steps of 16 (8 TMEM columns)
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts(t_dv, tmem + 128 * b + kk * 8, sdesc_sw128(db + kk * 2048, kQPanel, 1024), kIdescAcc,
+          mma_ts(t_dv, tmem + 128 * b + 16 + kk * 8, sdesc_sw128(db + kk * 2048, kQPanel, 1024), kIdescAcc,
                  (i > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts(t_dk, tmem + 128 * b + 64 + kk * 8, sdesc_sw128(qb + kk * 2048, kQPanel, 1024), kIdescAcc,
+          mma_ts(t_dk, tmem + 128 * b + 80 + kk * 8, sdesc_sw128(qb + kk * 2048, kQPanel, 1024), kIdescAcc,
                  (i > 0 || kk > 0));
         // dQ^T = K^T dS^T: K = 128 keys in 8 steps of 16 rows (2048 bytes)
         const uint32_t dsb = sb + kOffDS + b * kDSTile;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ss(tmem + 128 * b, sdesc_sw128(sb + kOffK + kk * 2048, kKVPanel, 1024),
+          mma_ss(tmem + 128 * b + 64, sdesc_sw128(sb + kOffK + kk * 2048, kKVPanel, 1024),
                  sdesc_sw128(dsb + kk * 2048, kKVPanel, 1024), kIdescDQ, kk > 0);
         tc_commit(bar(B_DQFULL + b));
         tc_commit(bar(B_DSEMPTY + b));
@@ -300,8 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* lse2 = vec + s * 2 * kBQ;
         const float* dis = lse2 + kBQ;
         uint32_t sv[32], dv[32];
-        tmem_ld32(lane_base + 128 * b + 32 * wg, sv);
-        tmem_ld32(lane_base + 128 * b + 64 + 32 * wg, dv);
+        tmem_ld32x2(lane_base + 128 * b + 32 * wg, lane_base + 128 * b + 64 + 32 * wg, sv, dv);
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -318,17 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pp[e] = pack_bf16(p0, p1);
           dd[e] = pack_bf16(d0, d1);
         }
-        // both warpgroups have read their S^T/dP^T columns before either overwrites
-        // columns the other reads (a bounded mbarrier wait, not a named barrier, so that a
-        // warp that gave up cannot leave the others waiting)
-        tc_fence_before();
-        mbar_arrive(bar(B_RDONE + b));
-        ok = mbar_wait(bar(B_RDONE + b), (step >> 1) & 1, abort_flag, a.err, kErrBwdWait + 12);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) return false;
-        tc_fence_after();
-        tmem_st16(lane_base + 128 * b + 16 * wg, pp);
-        tmem_st16(lane_base + 128 * b + 64 + 16 * wg, dd);
+        tmem_st16(lane_base + 128 * b + 16 + 16 * wg, pp);
+        tmem_st16(lane_base + 128 * b + 80 + 16 * wg, dd);
         // dS^T row r, queries [32 wg, 32 wg + 32): 16-byte chunks 4 wg .. 4 wg + 3 of the
         // 128-byte row, 128-byte swizzle (chunk XOR row & 7)
         uint8_t* drow = ds_row + b * kDSTile;
@@ -389,8 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) return false;
         tc_fence_after();
         uint32_t x0[32], x1[32];
-        tmem_ld32(lane_base + 128 * b, x0);
-        tmem_ld32(lane_base + 128 * b + 32, x1);
+        tmem_ld32x2(lane_base + 128 * b + 64, lane_base + 128 * b + 96, x0, x1);
         tc_fence_before();
         mbar_arrive(bar(B_DQEMPTY + b));  // TMEM buffer free; the adds run from registers
         const int q_valid = min(kBQ, itm.q_len - qs * kBQ);
