@@ -51,7 +51,7 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-constexpr int kMergeRows = 4;  // consecutive tokens per warp
+constexpr int kMergeRows = 8;  // consecutive tokens per warp
 
 template <int N>
 __device__ __forceinline__ void store_bf16(__nv_bfloat16* dst, const float (&x)[N], float inv) {
@@ -135,8 +135,7 @@ __global__ void __launch_bounds__(32 * kRowWarps)
   }
   const int P = start[R];
 
-  float acc[R][N];
-  float m[R], ws[R];
+  const long long obase = static_cast<long long>(blockIdx.y) * T;
   if (P <= kMergePairs) {
     // pair p = (row i, partial k): lane p knows its row and partial-row index
     int myrow = -1;
@@ -160,11 +159,9 @@ __global__ void __launch_bounds__(32 * kRowWarps)
     }
     // all partial rows in flight first, then the LSEs
     float x[kMergePairs][N];
-    int rowof[kMergePairs];
 #pragma unroll
     for (int p = 0; p < kMergePairs; ++p) {
       const long long pr = __shfl_sync(0xffffffffu, prow, p);
-      rowof[p] = __shfl_sync(0xffffffffu, myrow, p);
       if (p < P) {
         vload(reinterpret_cast<const typename V::F*>(part_o + pr * D) + lane, x[p]);
       } else {
@@ -173,42 +170,65 @@ __global__ void __launch_bounds__(32 * kRowWarps)
       }
     }
     const float l = lane < P ? __ldg(part_lse + prow) : -INFINITY;
-    float mine_m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      m[i] = warp_max(myrow == i ? l : -INFINITY);
-      if (myrow == i) mine_m = m[i];
-    }
-    const float w = (myrow >= 0 && l != -INFINITY) ? __expf(l - mine_m) : 0.f;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      ws[i] = warp_sum(myrow == i ? w : 0.f);
-#pragma unroll
-      for (int e = 0; e < N; ++e) acc[i][e] = 0.f;
-    }
-#pragma unroll
-    for (int p = 0; p < kMergePairs; ++p) {
-      const float wp = __shfl_sync(0xffffffffu, w, p);
+    if (P == R) {
+      // one partial per row (every row's range has a single run): the merge is the identity
+      // for rows with a finite LSE; rows without any visible key give O = 0, LSE = -inf
 #pragma unroll
       for (int i = 0; i < R; ++i) {
-        const float wi = (rowof[p] == i) ? wp : 0.f;
+        const long long t = t0 + i;
+        const float li = __shfl_sync(0xffffffffu, l, i);
+        if (t < T) {
+          store_bf16<N>(o + (obase + t) * D + lane * N, x[i], li == -INFINITY ? 0.f : 1.f);
+          if (lane == i) lse[obase + t] = li;
+        }
+      }
+    } else {
+      // per row: m = max lse, w = exp(lse - m), out = sum w x / sum w
+      float m_mine = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < N; ++e) acc[i][e] = fmaf(wi, x[p][e], acc[i][e]);
+      for (int i = 0; i < R; ++i) {
+        const float mi = warp_max(myrow == i ? l : -INFINITY);
+        if (myrow == i) m_mine = mi;
+      }
+      const float w = (myrow >= 0 && l != -INFINITY) ? __expf(l - m_mine) : 0.f;
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const long long t = t0 + i;
+        float acc[N];
+#pragma unroll
+        for (int e = 0; e < N; ++e) acc[e] = 0.f;
+        float ws = 0.f;
+#pragma unroll
+        for (int p = 0; p < kMergePairs; ++p) {
+          const float wp = __shfl_sync(0xffffffffu, w, p);
+          const int rp = __shfl_sync(0xffffffffu, myrow, p);
+          const float wi = (rp == i) ? wp : 0.f;
+          ws += wi;
+#pragma unroll
+          for (int e = 0; e < N; ++e) acc[e] = fmaf(wi, x[p][e], acc[e]);
+        }
+        const float mi = __shfl_sync(0xffffffffu, m_mine, start[i] < 32 ? start[i] : 0);
+        if (t < T) {
+          store_bf16<N>(o + (obase + t) * D + lane * N, acc, ws > 0.f ? 1.f / ws : 0.f);
+          if (lane == i) lse[obase + t] = ws > 0.f ? mi + logf(ws) : -INFINITY;
+        }
       }
     }
   } else {
-#pragma unroll
-    for (int i = 0; i < R; ++i) merge_row_general<D>(part_o, part_lse, off[i], stride[i], nr[i], lane, acc[i], m[i], ws[i]);
-  }
-
-  const long long obase = static_cast<long long>(blockIdx.y) * T;
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const long long t = t0 + i;
-    if (t >= T) break;
-    const float inv = ws[i] > 0.f ? 1.f / ws[i] : 0.f;
-    store_bf16<N>(o + (obase + t) * D + lane * N, acc[i], inv);
-    if (lane == i) lse[obase + t] = ws[i] > 0.f ? m[i] + logf(ws[i]) : -INFINITY;
+#pragma unroll 1
+    for (int i = 0; i < R; ++i) {
+      const long long t = t0 + i;
+      float acc[N];
+      float mi, wsi;
+      const long long oi = hoff + __shfl_sync(0xffffffffu, info.x, i);
+      const int si = __shfl_sync(0xffffffffu, info.y, i);
+      const int ni = __shfl_sync(0xffffffffu, info.z, i);
+      merge_row_general<D>(part_o, part_lse, oi, si, ni, lane, acc, mi, wsi);
+      if (t < T) {
+        store_bf16<N>(o + (obase + t) * D + lane * N, acc, wsi > 0.f ? 1.f / wsi : 0.f);
+        if (lane == 0) lse[obase + t] = wsi > 0.f ? mi + logf(wsi) : -INFINITY;
+      }
+    }
   }
 }
 
