@@ -262,15 +262,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sv[4][32];
+        uint32_t sv[128];
+        tmem_ld128(s_addr, sv);
+        // tiles with every column visible to every row of the warp take the short path
+        // (packed float32x2 arithmetic, 3-input max); diagonal and ragged tiles mask
+        const bool full = __all_sync(0xffffffffu, lim >= kTileN);
+        float mx;
+        if (full) {
+          float mc[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv[c]);
-        float mx = -INFINITY;
+          for (int c = 0; c < 4; ++c) {
+            mc[c] = __uint_as_float(sv[32 * c]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+            for (int e = 0; e < 15; ++e)
+              mc[c] = max3f(mc[c], __uint_as_float(sv[32 * c + 1 + 2 * e]), __uint_as_float(sv[32 * c + 2 + 2 * e]));
+            mc[c] = fmaxf(mc[c], __uint_as_float(sv[32 * c + 31]));
+          }
+          mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+        } else {
+          mx = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(sv[c][e]));
+          for (int e = 0; e < 128; ++e)
+            if (e < lim) mx = fmaxf(mx, __uint_as_float(sv[e]));
+        }
         const float m_new = fmaxf(m_used, mx * a.scale_log2);
         float alpha = 1.f;
         const bool grow = m_new > m_used + kRescaleThreshold;
@@ -280,18 +294,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         const float mb = (m_used == -INFINITY) ? 0.f : m_used;
         float rowsum = 0.f;
+        if (full) {
+          float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = c * 32 + 2 * e;
-            const float p0 = (c0 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c][2 * e]), a.scale_log2, -mb)) : 0.f;
-            const float p1 = (c0 + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c][2 * e + 1]), a.scale_log2, -mb)) : 0.f;
-            rowsum += p0 + p1;
-            pk[e] = pack_bf16(p0, p1);
+            for (int e = 0; e < 16; ++e) {
+              const int i0 = 32 * c + 2 * e;
+              const float2 x = ffma2(__uint_as_float(sv[i0]), __uint_as_float(sv[i0 + 1]), a.scale_log2, a.scale_log2,
+                                     -mb, -mb);
+              const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+              acc2 = fadd2(acc2.x, acc2.y, p0, p1);
+              pk[e] = pack_bf16(p0, p1);
+            }
+            tmem_st16(s_addr + c * 16, pk);
           }
-          tmem_st16(s_addr + c * 16, pk);
+          rowsum = acc2.x + acc2.y;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c0 = c * 32 + 2 * e;
+              const float p0 = (c0 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0]), a.scale_log2, -mb)) : 0.f;
+              const float p1 = (c0 + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), a.scale_log2, -mb)) : 0.f;
+              rowsum += p0 + p1;
+              pk[e] = pack_bf16(p0, p1);
+            }
+            tmem_st16(s_addr + c * 16, pk);
+          }
         }
         l = l * alpha + rowsum;
         // O holds the sum through key tile j-1 once PV(t, j-1) completes; rows whose maximum
