@@ -258,20 +258,22 @@ def cpu_baseline_sample(w, target_s=12.0):
             "seconds": dt}
 
 
-def traffic_from_profile(kernel_file, kernel_tag):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if the
-    kernel source has not changed since it was captured (sha256 recorded in the summary)."""
+def traffic_from_profile(kernel_tag, block):
+    """DRAM bytes per launch of a kernel on this workload from the committed ncu summary
+    (profiles/traffic.txt: tag, source file, sha256/16 of that file at capture, block size,
+    bytes), or None if the kernel's source has changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    src = os.path.join(ROOT, "context_parallelism_fcp_gb300", "csrc", kernel_file)
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
     with open(p) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and parts[0] == kernel_tag and parts[1] == sha:
-                return float(parts[2])
+            if len(parts) < 5 or parts[0].startswith("#") or parts[0] != kernel_tag or int(parts[3]) != block:
+                continue
+            src = os.path.join(ROOT, "context_parallelism_fcp_gb300", "csrc", parts[1])
+            with open(src, "rb") as g:
+                if hashlib.sha256(g.read()).hexdigest()[:16] == parts[2]:
+                    return float(parts[4])
     return None
 
 
@@ -329,8 +331,8 @@ def bench_fcp(args):
     dominant = "bwd" if phase["bwd"] >= phase["fwd"] else "fwd"
     dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
     dom_flops = step.bwd_flops if dominant == "bwd" else step.fwd_flops
-    traffic = traffic_from_profile("fcp_bwd.cu" if dominant == "bwd" else "fcp_fwd.cu",
-                                   "bwd_kernel" if dominant == "bwd" else "fwd_kernel")
+    traffic = traffic_from_profile("bwd_d128_kernel" if dominant == "bwd" else "fwd_kernel", w.block_size) \
+        if w.head_dim == 128 and args.seq_len == 32768 else None
     merge_gbs = step.merge_bytes / (phase["merge"] * 1e-3) / 1e9
 
     result = {
