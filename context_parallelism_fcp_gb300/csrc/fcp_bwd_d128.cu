@@ -213,36 +213,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 13) {
     // ---------------------------------------------------------------- MMA issuer
+    // the whole warp runs this with uniform operands; one elected lane issues each MMA/commit
     bool ok = !skip;
-    if (lane == 0) {
-      if (ok) ok = mbar_wait(bar(B_KVFULL), 0, abort_flag, a.err, kErrBwdWait + 2);
+    {
+      auto wwait = [&](uint32_t bb, uint32_t parity, int code) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bb, parity, abort_flag, a.err, code));
+      };
+      if (ok) ok = wwait(bar(B_KVFULL), 0, kErrBwdWait + 2);
       tc_fence_after();
       const uint32_t t_dv = tmem + 256, t_dk = tmem + 384;
       // number of steps, walked once without waiting
       const int total = ok ? for_each_step([](int, int, const fcp_item&, int) { return true; }) : 0;
       auto issue_sdp = [&](int j) -> bool {
         const int s = j % kStages, b = j & 1;
-        if (!mbar_wait(bar(B_QFULL + s), (j / kStages) & 1, abort_flag, a.err, kErrBwdWait + 3)) return false;
+        if (!wwait(bar(B_QFULL + s), (j / kStages) & 1, kErrBwdWait + 3)) return false;
         tc_fence_after();
         const uint32_t qb = sb + kOffQ + s * kQTile, db = sb + kOffDO + s * kQTile;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * kKVPanel + (kk & 3) * 32;
           const uint32_t qo = (kk >> 2) * kQPanel + (kk & 3) * 32;
-          mma_ss(tmem + 128 * b, sdesc_sw128(sb + kOffK + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), kIdescST,
+          mma_ss_w(tmem + 128 * b, sdesc_sw128(sb + kOffK + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), kIdescST,
                  kk > 0);
         }
         // the dP^T half of buffer b is free once the dQ^T of step j-2 has been read out of it
-        if (!mbar_wait(bar(B_DQEMPTY + b), ((j >> 1) & 1) ^ 1, abort_flag, a.err, kErrBwdWait + 4)) return false;
+        if (!wwait(bar(B_DQEMPTY + b), ((j >> 1) & 1) ^ 1, kErrBwdWait + 4)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * kKVPanel + (kk & 3) * 32;
           const uint32_t qo = (kk >> 2) * kQPanel + (kk & 3) * 32;
-          mma_ss(tmem + 128 * b + 64, sdesc_sw128(sb + kOffV + ko, 16, 1024), sdesc_sw128(db + qo, 16, 1024),
+          mma_ss_w(tmem + 128 * b + 64, sdesc_sw128(sb + kOffV + ko, 16, 1024), sdesc_sw128(db + qo, 16, 1024),
                  kIdescST, kk > 0);
         }
-        tc_commit(bar(B_STFULL + b));
+        tc_commit_w(bar(B_STFULL + b));
         return true;
       };
       if (ok && total > 0) ok = issue_sdp(0);
@@ -252,31 +256,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const int s = i % kStages, b = i & 1;
-        ok = mbar_wait(bar(B_DSFULL + b), (i >> 1) & 1, abort_flag, a.err, kErrBwdWait + 5);
+        ok = wwait(bar(B_DSFULL + b), (i >> 1) & 1, kErrBwdWait + 5);
         if (!ok) break;
         tc_fence_after();
         const uint32_t qb = sb + kOffQ + s * kQTile, db = sb + kOffDO + s * kQTile;
         // dV += P^T dO and dK += dS^T Q: K = 64 queries in 4 steps of 16 (8 TMEM columns)
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts(t_dv, tmem + 128 * b + 16 + kk * 8, sdesc_sw128(db + kk * 2048, kQPanel, 1024), kIdescAcc,
+          mma_ts_w(t_dv, tmem + 128 * b + 16 + kk * 8, sdesc_sw128(db + kk * 2048, kQPanel, 1024), kIdescAcc,
                  (i > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts(t_dk, tmem + 128 * b + 80 + kk * 8, sdesc_sw128(qb + kk * 2048, kQPanel, 1024), kIdescAcc,
+          mma_ts_w(t_dk, tmem + 128 * b + 80 + kk * 8, sdesc_sw128(qb + kk * 2048, kQPanel, 1024), kIdescAcc,
                  (i > 0 || kk > 0));
         // dQ^T = K^T dS^T: K = 128 keys in 8 steps of 16 rows (2048 bytes)
         const uint32_t dsb = sb + kOffDS + b * kDSTile;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ss(tmem + 128 * b + 64, sdesc_sw128(sb + kOffK + kk * 2048, kKVPanel, 1024),
+          mma_ss_w(tmem + 128 * b + 64, sdesc_sw128(sb + kOffK + kk * 2048, kKVPanel, 1024),
                  sdesc_sw128(dsb + kk * 2048, kKVPanel, 1024), kIdescDQ, kk > 0);
-        tc_commit(bar(B_DQFULL + b));
-        tc_commit(bar(B_DSEMPTY + b));
-        tc_commit(bar(B_QEMPTY + s));
+        tc_commit_w(bar(B_DQFULL + b));
+        tc_commit_w(bar(B_DSEMPTY + b));
+        tc_commit_w(bar(B_QEMPTY + s));
       }
       n_steps = total;
-      tc_commit(bar(B_ACCDONE));
+      tc_commit_w(bar(B_ACCDONE));
     }
   } else if (warp < 8) {
     // ---------------------------------------------------------------- gradient warps

@@ -171,7 +171,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && !skip) {
+    // the whole warp runs this with uniform operands; one elected lane issues each MMA/commit
+    if (!skip) {
+      auto wwait = [&](uint32_t bb, uint32_t parity, int code) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bb, parity, abort_flag, a.err, code));
+      };
       auto issue_s = [&](int t, int s) {
         const uint32_t d = tmem + t * 128;
         const uint32_t qbase = sb + (t ? C::kQ1 : C::kQ0);
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(d, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::kIdescS, kk > 0);
+          mma_ss_w(d, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::kIdescS, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
@@ -188,9 +192,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t vbase = sb + C::kV + s * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts(d, p + kk * 8, sdesc_sw128(vbase + kk * 2048, kPanelBytes, 1024), C::kIdescPV, (acc || kk > 0));
+          mma_ts_w(d, p + kk * 8, sdesc_sw128(vbase + kk * 2048, kPanelBytes, 1024), C::kIdescPV, (acc || kk > 0));
       };
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.err, kErrFwdWait + 3);
+      bool ok = wwait(bar(B_QFULL), 0, kErrFwdWait + 3);
       tc_fence_after();
       int j = 0;
       for (int ii = run.item_begin; ii < run.item_end && ok; ++ii) {
@@ -199,46 +203,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int kt = 0; kt < nkt && ok; ++kt, ++j) {
           const int s = j & 1;
           const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait(bar(B_KFULL + s), ph, abort_flag, a.err, kErrFwdWait + 4)) { ok = false; break; }
+          if (!wwait(bar(B_KFULL + s), ph, kErrFwdWait + 4)) { ok = false; break; }
           tc_fence_after();
           for (int t = 0; t < 2; ++t) {
             if (j > 0) {
               const int ps = (j - 1) & 1;
               if (t == 0) {
-                if (!mbar_wait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, abort_flag, a.err, kErrFwdWait + 5)) {
+                if (!wwait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, kErrFwdWait + 5)) {
                   ok = false;
                   break;
                 }
               }
-              if (!mbar_wait(bar(B_PFULL + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 6)) {
+              if (!wwait(bar(B_PFULL + t), (j - 1) & 1, kErrFwdWait + 6)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               issue_pv(t, ps, j - 1 > 0);
-              tc_commit(bar(B_ODONE + t));
-              if (t == 1) tc_commit(bar(B_VEMPTY + ps));
+              tc_commit_w(bar(B_ODONE + t));
+              if (t == 1) tc_commit_w(bar(B_VEMPTY + ps));
             }
             issue_s(t, s);
-            tc_commit(bar(B_SFULL + t));
+            tc_commit_w(bar(B_SFULL + t));
           }
-          if (ok) tc_commit(bar(B_KEMPTY + s));
+          if (ok) tc_commit_w(bar(B_KEMPTY + s));
         }
       }
       if (ok && j > 0) {
         const int ps = (j - 1) & 1;
-        ok = mbar_wait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, abort_flag, a.err, kErrFwdWait + 5);
+        ok = wwait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, kErrFwdWait + 5);
         for (int t = 0; t < 2 && ok; ++t) {
-          ok = mbar_wait(bar(B_PFULL + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 6);
+          ok = wwait(bar(B_PFULL + t), (j - 1) & 1, kErrFwdWait + 6);
           if (!ok) break;
           tc_fence_after();
           issue_pv(t, ps, j - 1 > 0);
-          tc_commit(bar(B_ODONE + t));
+          tc_commit_w(bar(B_ODONE + t));
         }
       }
       // every issued MMA has completed once the drain barrier fires
-      tc_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, abort_flag, a.err, kErrFwdWait + 7);
+      tc_commit_w(bar(B_DRAIN));
+      wwait(bar(B_DRAIN), 0, kErrFwdWait + 7);
     }
   } else if (!skip) {
     // ------------------------------------------------------------ softmax (warps 0-7)
