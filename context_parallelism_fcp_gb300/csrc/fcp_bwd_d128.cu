@@ -51,7 +51,9 @@ constexpr int kOffQ = 2 * kKVTile;                          // kStages tiles
 constexpr int kOffDO = kOffQ + kStages * kQTile;            // kStages tiles
 constexpr int kOffDS = kOffDO + kStages * kQTile;           // 2 buffers
 constexpr int kOffVec = kOffDS + 2 * kDSTile;               // kStages x (lse2[64], di[64])
-constexpr int kOffBar = kOffVec + kStages * 2 * kBQ * 4;
+constexpr int kOffStage = ((kOffVec + kStages * 2 * kBQ * 4) + 1023) & ~1023;  // dQ [64 q][128 d] float32
+constexpr int kStageBytes = kBQ * kD * 4;
+constexpr int kOffBar = kOffStage + kStageBytes;
 constexpr int kSmemBytes = kOffBar + 256;
 
 // mbarrier indices, laid out from the stage count so that no two ever share a slot
@@ -65,10 +67,12 @@ enum : int {
   B_DQFULL = B_DSEMPTY + 2,        // 2 buffers
   B_DQEMPTY = B_DQFULL + 2,        // 2 buffers
   B_ACCDONE = B_DQEMPTY + 2,
-  B_COUNT = B_ACCDONE + 1
+  B_STGFULL = B_ACCDONE + 1,       // the dQ staging tile is written
+  B_STGFREE = B_STGFULL + 1,       // the previous reduce has read the staging tile
+  B_COUNT = B_STGFREE + 1
 };
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
-static_assert(kOffVec + kStages * 2 * kBQ * 4 == kOffBar, "vector area");
+static_assert(kOffVec + kStages * 2 * kBQ * 4 <= kOffStage, "vector area");
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // S^T, dP^T: M = 128 keys, N = 64 queries, both operands K-major.
@@ -96,7 +100,8 @@ struct Args {
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_d128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const Args a) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmDQ, const Args a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) atomicCAS(a.err, 0, kErrSmemAlign);
@@ -132,6 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_DQEMPTY + b), 128);
     }
     mbar_init(bar(B_ACCDONE), 1);
+    mbar_init(bar(B_STGFULL), 128);
+    mbar_init(bar(B_STGFREE), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
     mbar_fence_init();
   }
@@ -307,25 +314,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) return false;
         tc_fence_after();
-        const float* lse2 = vec + s * 2 * kBQ;
-        const float* dis = lse2 + kBQ;
+        const float* lse2 = vec + s * 2 * kBQ + 32 * wg;  // this warpgroup's 32 columns
+        const float* dis = vec + s * 2 * kBQ + kBQ + 32 * wg;
         uint32_t sv[32], dv[32];
         tmem_ld32x2(lane_base + 128 * b + 32 * wg, lane_base + 128 * b + 64 + 32 * wg, sv, dv);
         uint32_t pp[16], dd[16];
+        if (__all_sync(0xffffffffu, qmin <= 32 * wg)) {
+          // every column visible: packed float32x2 arithmetic, LSE/Di as 16-byte loads
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = 32 * wg + 2 * e;
-          float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
-          if (c0 >= qmin) {
-            p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * e]), a.scale_log2, -lse2[c0]));
-            d0 = p0 * (__uint_as_float(dv[2 * e]) - dis[c0]);
+          for (int k = 0; k < 8; ++k) {
+            const float4 l4 = reinterpret_cast<const float4*>(lse2)[k];
+            const float4 d4 = reinterpret_cast<const float4*>(dis)[k];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * k + h;
+              const float l0 = h ? l4.z : l4.x, l1 = h ? l4.w : l4.y;
+              const float i0 = h ? d4.z : d4.x, i1 = h ? d4.w : d4.y;
+              const float2 x = ffma2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), a.scale_log2,
+                                     a.scale_log2, -l0, -l1);
+              const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+              const float2 g = fsub2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1]), i0, i1);
+              const float2 ds = fmul2(p0, p1, g.x, g.y);
+              pp[e] = pack_bf16(p0, p1);
+              dd[e] = pack_bf16(ds.x, ds.y);
+            }
           }
-          if (c0 + 1 >= qmin) {
-            p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), a.scale_log2, -lse2[c0 + 1]));
-            d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - dis[c0 + 1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = 32 * wg + 2 * e;
+            float p0 = 0.f, p1 = 0.f, d0 = 0.f, d1 = 0.f;
+            if (c0 >= qmin) {
+              p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * e]), a.scale_log2, -lse2[2 * e]));
+              d0 = p0 * (__uint_as_float(dv[2 * e]) - dis[2 * e]);
+            }
+            if (c0 + 1 >= qmin) {
+              p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), a.scale_log2, -lse2[2 * e + 1]));
+              d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - dis[2 * e + 1]);
+            }
+            pp[e] = pack_bf16(p0, p1);
+            dd[e] = pack_bf16(d0, d1);
           }
-          pp[e] = pack_bf16(p0, p1);
-          dd[e] = pack_bf16(d0, d1);
         }
         tmem_st16(lane_base + 128 * b + 16 + 16 * wg, pp);
         tmem_st16(lane_base + 128 * b + 80 + 16 * wg, dd);
@@ -378,10 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- dQ drain (warps 8-11)
+    // dQ^T (lane = channel) goes into a [64 q][128 d] float32 staging tile; one lane adds the
+    // tile to the accumulator with a TMA reduce. Query rows past the item's range carry exact
+    // zeros (their P and dS are 0), and rows past T are clipped by the tensor map.
     bool ok = !skip;
     const int d = (warp & 3) * 32 + lane;  // channel = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const bool issuer = threadIdx.x == 8 * 32;
+    float* stage = reinterpret_cast<float*>(smem + kOffStage);
     if (ok) {
+      if (issuer) tma_prefetch_desc(&tmDQ);
       n_steps = for_each_step([&](const int step, const int h, const fcp_item& itm, const int qs) -> bool {
         const int b = step & 1;
         ok = mbar_wait(bar(B_DQFULL + b), (step >> 1) & 1, abort_flag, a.err, kErrBwdWait + 11);
@@ -391,17 +426,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t x0[32], x1[32];
         tmem_ld32x2(lane_base + 128 * b + 64, lane_base + 128 * b + 96, x0, x1);
         tc_fence_before();
-        mbar_arrive(bar(B_DQEMPTY + b));  // TMEM buffer free; the adds run from registers
-        const int q_valid = min(kBQ, itm.q_len - qs * kBQ);
-        float* dst = a.dq_acc + (static_cast<long long>(h) * a.T + itm.q_tok0 + qs * kBQ) * kD + d;
+        mbar_arrive(bar(B_DQEMPTY + b));  // TMEM buffer free
+        // the staging tile is free once the previous step's reduce has read it
+        ok = mbar_wait(bar(B_STGFREE), (step & 1) ^ 1, abort_flag, a.err, kErrBwdWait + 12);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (q < q_valid) atomicAdd(dst + static_cast<long long>(q) * kD, __uint_as_float(x0[q]));
+        for (int q = 0; q < 32; ++q) stage[q * kD + d] = __uint_as_float(x0[q]);
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (32 + q < q_valid) atomicAdd(dst + static_cast<long long>(32 + q) * kD, __uint_as_float(x1[q]));
+        for (int q = 0; q < 32; ++q) stage[(32 + q) * kD + d] = __uint_as_float(x1[q]);
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_STGFULL));
+        if (issuer) {
+          ok = mbar_wait(bar(B_STGFULL), step & 1, abort_flag, a.err, kErrBwdWait + 13);
+          if (ok) {
+            tma_reduce_add_3d(&tmDQ, sb + kOffStage, 0, itm.q_tok0 + qs * kBQ, h);
+            bulk_commit_group();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(bar(B_STGFREE));
+        }
         return true;
       });
+      if (issuer) bulk_wait_all();
     }
   }
 
@@ -426,8 +473,9 @@ fcp_status launch_bwd_d128(const fcp_plan* plan, const void* d_plan, const void*
   const DevLayout& L = plan->layout;
   if (L.n_bwd_units == 0) return FCP_OK;
   const int64_t T = plan->total_tokens;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   fcp_status st;
+  if ((st = make_f32x128_map(&mdq, dq_acc, hq, T, kBQ)) != FCP_OK) return st;
   if ((st = make_bf16_map(&mq, q, hq, T, kD, kBQ)) != FCP_OK) return st;
   if ((st = make_bf16_map(&mk, k, hkv, T, kD, kBN)) != FCP_OK) return st;
   if ((st = make_bf16_map(&mv, v, hkv, T, kD, kBN)) != FCP_OK) return st;
@@ -452,7 +500,7 @@ fcp_status launch_bwd_d128(const fcp_plan* plan, const void* d_plan, const void*
                "bwd d128 smem attribute");
   const long long grid = static_cast<long long>(L.n_bwd_units) * hkv;
   if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
-  bwd_d128_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, a);
+  bwd_d128_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
   FCP_CUDA_TRY(cudaGetLastError(), "bwd d128 launch");
   return FCP_OK;
 }

@@ -62,6 +62,28 @@ inline fcp_status make_bf16_map(CUtensorMap* map, const void* base, int heads, i
   return FCP_OK;
 }
 
+// Tensor map over a contiguous float32 tensor [heads, T, 128] with box {128, rows, 1}, no
+// swizzle: one box is `rows` tokens x 128 channels (512 bytes per row).
+inline fcp_status make_f32x128_map(CUtensorMap* map, const void* base, int heads, int64_t T, int rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) {
+    set_last_error("cuTensorMapEncodeTiled unavailable from the driver");
+    return FCP_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {128 * 4, static_cast<cuuint64_t>(T) * 128 * 4};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_last_error("cuTensorMapEncodeTiled (float32) failed with CUresult " + std::to_string(static_cast<int>(r)));
+    return FCP_ERR_CUDA;
+  }
+  return FCP_OK;
+}
+
 template <class T>
 inline const T* dev_array(const void* d_plan, size_t off) {
   return reinterpret_cast<const T*>(static_cast<const uint8_t*>(d_plan) + off);

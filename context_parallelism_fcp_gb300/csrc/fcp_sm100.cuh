@@ -91,6 +91,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// 3-D tiled reduce-add of a shared-memory box into global memory (bulk-group completion).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk operation of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk operation of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -256,6 +269,34 @@ __device__ __forceinline__ float2 fadd2(float a0, float a1, float b0, float b1) 
       "mov.b64 pa, {%2, %3};\n"
       "mov.b64 pb, {%4, %5};\n"
       "add.rn.f32x2 pd, pa, pb;\n"
+      "mov.b64 {%0, %1}, pd;\n"
+      "}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  return d;
+}
+
+// (a0, a1) - (b0, b1) and (a0, a1) * (b0, b1) as packed float32x2 operations.
+__device__ __forceinline__ float2 fsub2(float a0, float a1, float b0, float b1) {
+  float2 d;
+  asm("{\n"
+      ".reg .b64 pa, pb, pd;\n"
+      "mov.b64 pa, {%2, %3};\n"
+      "mov.b64 pb, {%4, %5};\n"
+      "sub.rn.f32x2 pd, pa, pb;\n"
+      "mov.b64 {%0, %1}, pd;\n"
+      "}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float a0, float a1, float b0, float b1) {
+  float2 d;
+  asm("{\n"
+      ".reg .b64 pa, pb, pd;\n"
+      "mov.b64 pa, {%2, %3};\n"
+      "mov.b64 pb, {%4, %5};\n"
+      "mul.rn.f32x2 pd, pa, pb;\n"
       "mov.b64 {%0, %1}, pd;\n"
       "}\n"
       : "=f"(d.x), "=f"(d.y)
