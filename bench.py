@@ -383,6 +383,8 @@ def bench_fcp(args):
 
     if not args.no_sweep:
         result["sweep"] = sweep(torch, fcp, W, args, dev, stream, flush, sustained)
+    if rank == 0:
+        result["solver"] = solver_report(fcp, W)
     if cpu is not None:
         result["cpu_baseline"] = cpu
     if rank == 0:
@@ -447,6 +449,25 @@ def sweep(torch, fcp, W, args, dev, stream, flush, sustained):
                         "fwd_bwd_frac_of_peak": round(tot / sustained, 4)})
             del st
             torch.cuda.empty_cache()
+    return out
+
+
+def solver_report(fcp, W):
+    """Host time of the congestion-free solver on the pages' cluster setting (256 workers,
+    32K tokens each, 4K blocks) and on the benchmark's own plan."""
+    out = {}
+    for name, w in (("cluster_256x32k", W.cluster_batch()), ("bench_32k", W.block_sweep(HEADLINE_BLOCK))):
+        t0 = time.perf_counter()
+        plan = fcp.Plan(w.seqlens, w.block_size, w.causal).distribute(w.n_workers, w.token_cap)
+        t1 = time.perf_counter()
+        res = plan.solve()
+        t2 = time.perf_counter()
+        loads = [int(x) for x in plan.view()["load"]]
+        mx = max(loads)
+        out[name] = {"workers": w.n_workers, "blocks": plan.view()["n_blocks"], "transfers": int(len(res["transfers"])),
+                     "stages": res["n_stages"], "plan_ms": round((t1 - t0) * 1e3, 2),
+                     "solve_ms": round((t2 - t1) * 1e3, 2),
+                     "imbalance": round((mx - sum(loads) / len(loads)) / mx, 6) if mx else 0.0}
     return out
 
 

@@ -77,6 +77,10 @@ class _Run(ctypes.Structure):
                                               "part_row0", "reserved")]
 
 
+class _Transfer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("kv_block", "src", "dst", "stage", "tokens", "reserved")]
+
+
 class _View(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_seqs", "n_blocks", "n_segs", "n_items", "n_runs", "n_workers",
                                               "block_size", "causal", "coalesce", "distributed")] + [
@@ -103,6 +107,9 @@ _SIGNATURES = {
     "fcp_distribute": (_ST, [_P, _I32, _I64]),
     "fcp_coalesce": (_ST, [_P, _I32]),
     "fcp_plan_query": (_ST, [_P, ctypes.POINTER(_View)]),
+    "fcp_solve_stages": (_ST, [_P]),
+    "fcp_plan_transfers": (_ST, [_P, ctypes.POINTER(ctypes.POINTER(_Transfer)), ctypes.POINTER(_I32),
+                                 ctypes.POINTER(_I32)]),
     "fcp_plan_device_bytes": (_SZ, [_P]),
     "fcp_plan_upload": (_ST, [_P, _P, _SZ, _P]),
     "fcp_partial_sizes": (_ST, [_P, _I32, _I32, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
@@ -195,6 +202,18 @@ class Plan:
     def coalesce(self, degree: int) -> "Plan":
         _check(lib().fcp_coalesce(self._h, int(degree)), "fcp_coalesce")
         return self
+
+    def solve(self) -> dict:
+        """Congestion-free sub-stages (fcp_solve_stages): transfers as rows (kv_block, src, dst,
+        stage, tokens) and the number of stages."""
+        L = lib()
+        _check(L.fcp_solve_stages(self._h), "fcp_solve_stages")
+        ptr = ctypes.POINTER(_Transfer)()
+        n, st = _I32(), _I32()
+        _check(L.fcp_plan_transfers(self._h, ctypes.byref(ptr), ctypes.byref(n), ctypes.byref(st)),
+               "fcp_plan_transfers")
+        rows = _arr(ptr, n.value, None, ("kv_block", "src", "dst", "stage", "tokens"))
+        return {"transfers": rows, "n_stages": int(st.value)}
 
     def view(self) -> dict:
         v = _View()

@@ -85,6 +85,11 @@ struct fcp_plan {
   std::vector<fcp_run> runs;
   int64_t partial_rows = 0;
 
+  // Congestion-free solver output (fcp_solve_stages).
+  bool solved = false;
+  std::vector<fcp_transfer> transfers;
+  int32_t n_stages = 0;
+
   // Host copy of the device image, rebuilt after distribute/coalesce.
   std::vector<uint8_t> image;
   fcp::DevLayout layout;

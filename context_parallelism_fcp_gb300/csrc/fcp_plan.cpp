@@ -372,6 +372,9 @@ fcp_status fcp_distribute(fcp_plan* p, int32_t n_workers, int64_t token_cap) {
   p->load = std::move(load);
   p->tokens = std::move(tokens);
   p->distributed = true;
+  p->solved = false;
+  p->transfers.clear();
+  p->n_stages = 0;
   build_runs(p, 1);
   if (!build_image(p)) {
     p->distributed = false;

@@ -81,6 +81,13 @@ typedef struct {
   int32_t worker, q_block, q_tok0, q_len, item_begin, item_end, part_row0, reserved;
 } fcp_run;
 
+/* One block transfer of the communication plan: KV block kv_block moves from its owner
+ * src to worker dst (which owns a Q block that attends to it), in congestion-free
+ * sub-stage `stage`. tokens is the block's length. */
+typedef struct {
+  int32_t kv_block, src, dst, stage, tokens, reserved;
+} fcp_transfer;
+
 typedef struct fcp_plan fcp_plan;
 
 /* Read-only view of a host plan. Pointers stay valid until the next mutating call on
@@ -124,6 +131,22 @@ fcp_status fcp_distribute(fcp_plan* plan, int32_t n_workers, int64_t token_cap);
  * gives one partial per (Q-block, KV-block) pair. Errors: FCP_ERR_INVALID (degree <= 0),
  * FCP_ERR_STATE (not distributed). */
 fcp_status fcp_coalesce(fcp_plan* plan, int32_t degree);
+
+/* Congestion-free solver (Section 4.2, "Congestion-free solver"; Lemmas 1 and 2; Figure 8):
+ * builds the data-flow bipartite multigraph of a distributed plan -- one edge S(src) ->
+ * R(dst) per distinct (KV block, receiving worker) whose block is owned elsewhere, in
+ * work-list order -- and partitions its edges into Delta disjoint matchings, Delta being
+ * the maximum number of blocks any worker sends or receives (the optimum: a stage is a
+ * matching, Lemma 1, and the busiest worker needs Delta stages, Lemma 2). The graph is
+ * padded to Delta-regular with dummy edges and perfect matchings are peeled off with
+ * Hopcroft-Karp. Results: fcp_plan_transfers. Errors: FCP_ERR_INVALID, FCP_ERR_STATE (not
+ * distributed). Recomputed by each call; cleared by fcp_distribute. */
+fcp_status fcp_solve_stages(fcp_plan* plan);
+
+/* Read-only access to the solver's result: *transfers (n_transfers entries, valid until
+ * the next mutating call) and the number of sub-stages. FCP_ERR_STATE if not solved. */
+fcp_status fcp_plan_transfers(const fcp_plan* plan, const fcp_transfer** transfers, int32_t* n_transfers,
+                              int32_t* n_stages);
 
 /* Fill *view with read-only pointers into the plan. */
 fcp_status fcp_plan_query(const fcp_plan* plan, fcp_plan_view* view);

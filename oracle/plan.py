@@ -211,3 +211,48 @@ def imbalance(load: Sequence[int]) -> float:
     if mx == 0:
         return 0.0
     return (mx - sum(load) / len(load)) / mx
+
+
+def transfers(part: Dict[str, list], dist: Dict[str, list]) -> List[tuple]:
+    """Edges of the data-flow bipartite graph (Section 4.2, congestion-free solver; Figure 8):
+    one (kv_block, src, dst, tokens) per distinct (KV block, receiving worker) where the
+    block's owner src differs from the worker dst whose Q block attends to it, in work-list
+    order (a worker pulls each remote block once)."""
+    owner = dist["worker_of_block"]
+    seen = set()
+    out = []
+    for (w, qb, kb, *_rest) in dist["items"]:
+        src = owner[kb]
+        if src == w or (kb, w) in seen:
+            continue
+        seen.add((kb, w))
+        out.append((kb, src, w, part["blocks"][kb][2]))
+    return out
+
+
+def max_degree(edges: Sequence[tuple], n_workers: int) -> int:
+    """Delta: the largest number of blocks one worker sends or receives. By Lemma 1 a
+    congestion-free sub-stage is a matching, by Lemma 2 the busiest worker needs Delta of
+    them, and a bipartite multigraph's edges split into exactly Delta matchings."""
+    if not edges:
+        return 0
+    send = [0] * n_workers
+    recv = [0] * n_workers
+    for e in edges:
+        send[e[1]] += 1
+        recv[e[2]] += 1
+    return max(max(send), max(recv))
+
+
+def stages_are_matchings(edges: Sequence[tuple], stage: Sequence[int], n_stages: int) -> bool:
+    """Every edge has a stage in [0, n_stages) and no worker sends or receives two blocks in
+    the same stage."""
+    sent, got = set(), set()
+    for e, s in zip(edges, stage):
+        if not 0 <= s < n_stages:
+            return False
+        if (s, e[1]) in sent or (s, e[2]) in got:
+            return False
+        sent.add((s, e[1]))
+        got.add((s, e[2]))
+    return True

@@ -221,3 +221,52 @@ def test_invalid_arguments():
         P.distribute(P.partition([4], 2, True), 0)
     empty = P.partition([], 4, True)
     assert empty["blocks"] == [] and P.distribute(empty, 3)["items"] == []
+
+
+def test_transfers_hand_worked():
+    """One causal sequence of 4 blocks on 2 workers: Zig-Zag gives w0 = {0, 3}, w1 = {1, 2}.
+    In work-list order (worker 0's items first): block 3 (w0) pulls KV 1 and KV 2 from w1;
+    block 1 (w1) pulls KV 0 from w0; block 2 (w1) holds KV 1 and 2 and pulls KV 0, which w1
+    already has. Worker 1 sends 2 blocks: Delta = 2."""
+    part = P.partition([8], 2, True)
+    dist = P.distribute(part, 2)
+    assert dist["worker_of_block"] == [0, 1, 1, 0]
+    edges = P.transfers(part, dist)
+    assert edges == [(1, 1, 0, 2), (2, 1, 0, 2), (0, 0, 1, 2)]
+    assert P.max_degree(edges, 2) == 2
+    assert P.stages_are_matchings(edges, [0, 1, 0], 2)
+    assert not P.stages_are_matchings(edges, [1, 1, 0], 2)  # worker 1 sends twice in stage 1
+
+
+def _min_matchings(edges, n):
+    """Smallest k such that the edges split into k matchings, by exhaustive search."""
+    if not edges:
+        return 0
+    for k in range(1, len(edges) + 1):
+        for assign in itertools.product(range(k), repeat=len(edges)):
+            if P.stages_are_matchings([(0,) + e for e in edges], assign, k):
+                return k
+    return len(edges)
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_min_congestion_free_stages_is_max_degree(seed):
+    """Lemmas 1-2 and Konig's theorem: the fewest sub-stages (matchings) covering a bipartite
+    multigraph's edges equals its maximum degree -- checked by brute force on tiny graphs."""
+    import random
+
+    r = random.Random(seed)
+    n = r.randint(2, 4)
+    edges = [(r.randrange(n), r.randrange(n)) for _ in range(r.randint(0, 6))]
+    edges = [e for e in edges if e[0] != e[1]] or edges[:0]
+    assert _min_matchings(edges, n) == P.max_degree([(0,) + e for e in edges], n)
+
+
+def test_every_remote_pair_has_a_transfer():
+    for seqlens, b, causal, n in _tiny_cases():
+        part = P.partition(seqlens, b, causal)
+        dist = P.distribute(part, n)
+        have = {(e[0], e[2]) for e in P.transfers(part, dist)}
+        for (w, qb, kb, *_rest) in dist["items"]:
+            if dist["worker_of_block"][kb] != w:
+                assert (kb, w) in have

@@ -112,3 +112,46 @@ def test_device_image_sizes(fcp):
     rows = plan.view()["partial_rows"]
     assert o == w.hq * rows * w.head_dim * 4 and l == w.hq * rows * 4
     assert plan.workspace_bytes(w.hq, w.head_dim) >= w.hq * w.total_tokens * (w.head_dim + 1) * 4
+
+
+def _solver_case(fcp, seqlens, b, causal, n, cap=None):
+    part = P.partition(seqlens, b, causal)
+    try:
+        dist = P.distribute(part, n, cap)
+    except P.CapacityError:
+        return
+    plan = fcp.Plan(seqlens, b, causal).distribute(n, cap)
+    res = plan.solve()
+    edges = P.transfers(part, dist)
+    got = res["transfers"]
+    assert len(got) == len(edges)
+    if edges:
+        assert np.array_equal(got[:, [0, 1, 2, 4]], np.array(edges, dtype=np.int64))
+    delta = P.max_degree(edges, n)
+    assert res["n_stages"] == delta
+    assert P.stages_are_matchings(edges, [int(x) for x in got[:, 3]] if len(got) else [], delta)
+
+
+@pytest.mark.parametrize("make", [W.tiny_causal, W.full_mask, W.causal_mixed, W.long_causal]
+                         + [lambda b=b: W.block_sweep(b) for b in W.SWEEP_BLOCK_SIZES])
+def test_solver_on_named_workloads(fcp, make):
+    w = make()
+    _solver_case(fcp, w.seqlens, w.block_size, w.causal, w.n_workers, w.token_cap)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_solver_on_random_batches(fcp, seed):
+    r = random.Random(1000 + seed)
+    b = r.choice([1, 2, 4, 64, 100])
+    seqlens = [r.choice([r.randint(1, b), r.randint(1, 6 * b), 3 * b]) for _ in range(r.randint(1, 10))]
+    _solver_case(fcp, seqlens, b, r.random() < 0.6, r.randint(1, 12))
+
+
+def test_solver_state_errors(fcp):
+    p = fcp.Plan([100], 10, True)
+    with pytest.raises(fcp.FcpError) as e:
+        p.solve()
+    assert e.value.status == 5
+    p.distribute(1)  # one worker: nothing moves
+    res = p.solve()
+    assert res["n_stages"] == 0 and len(res["transfers"]) == 0

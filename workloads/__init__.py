@@ -27,6 +27,7 @@ __all__ = [
     "long_causal",
     "block_sweep",
     "small_cases",
+    "cluster_batch",
     "make_qkv",
     "make_dout",
     "make_partials",
@@ -118,6 +119,24 @@ def block_sweep(block_size: int) -> Workload:
 
 
 SWEEP_BLOCK_SIZES = (512, 1024, 2048, 4096, 8192)
+
+
+def cluster_batch(n_workers: int = 256, tokens_per_worker: int = 32768, seed: int = 0) -> Workload:
+    """A cluster-scale batch in the pages' evaluation setting (Section 6.1: 32K tokens per GPU,
+    causal, 4K blocks, lengths long-tailed up to 512K): lognormal(ln 8192, 1.5) lengths
+    clipped to [128, 524288], drawn until n_workers * tokens_per_worker tokens (the last draw
+    truncated). Used for plan-level measurements (solver, balance), not for kernels."""
+    rng = np.random.default_rng(seed)
+    total = n_workers * tokens_per_worker
+    lens: List[int] = []
+    t = 0
+    while t < total:
+        v = int(np.clip(rng.lognormal(mean=np.log(8192.0), sigma=1.5), 128.0, 524288.0))
+        v = min(v, total - t)
+        lens.append(v)
+        t += v
+    return Workload(f"cluster {n_workers}x{tokens_per_worker}", lens, 4096, 64, 8, 128, n_workers, True,
+                    backward=False, seed=seed)
 
 
 def small_cases() -> List[Workload]:
