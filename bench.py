@@ -381,6 +381,7 @@ def bench_fcp(args):
     if not args.no_e2e:
         result["e2e"] = e2e(torch, fcp, w, args, dev, stream, step)
 
+    result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
     if not args.no_sweep:
         result["sweep"] = sweep(torch, fcp, W, args, dev, stream, flush, sustained)
     if rank == 0:
@@ -450,6 +451,27 @@ def sweep(torch, fcp, W, args, dev, stream, flush, sustained):
             del st
             torch.cuda.empty_cache()
     return out
+
+
+def reshuffle_bench(torch, fcp, step, stream, flush, pk):
+    """GB/s of the transparent reshuffle of Q (user -> worker layout and back), 2 bytes read
+    and written per element, L2 flushed before each timed launch."""
+    dst = torch.empty_like(step.q)
+    times = []
+    for i in range(6):
+        with torch.cuda.stream(stream):
+            flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fcp.reshuffle(step.plan, step.d_plan, step.q, dst, to_workers=(i % 2 == 0), stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(e0.elapsed_time(e1))
+    nbytes = 2 * step.q.numel() * step.q.element_size()
+    gbs = nbytes / (statistics.mean(times) * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": nbytes, "kernel": "reshuffle_kernel"}
 
 
 def solver_report(fcp, W):

@@ -31,6 +31,7 @@ __all__ = [
     "block_attn_bwd_prologue",
     "block_attn_bwd_tiles",
     "block_attn_bwd_dq_convert",
+    "reshuffle",
     "FcpAttention",
     "MASK_FULL",
     "MASK_CAUSAL_DIAG",
@@ -122,6 +123,7 @@ _SIGNATURES = {
     "fcp_block_attn_bwd_dq_convert": (_ST, [_P, _P, _I32, _I32, _P, _P]),
     "fcp_bwd_static_scratch_bytes": (_SZ, []),
     "fcp_block_attn_bwd_static_scratch": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "fcp_reshuffle": (_ST, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
     "fcp_device_error": (_ST, [_P, ctypes.POINTER(_I32), _P]),
     "fcp_plan_free": (None, [_P]),
     "fcp_status_string": (ctypes.c_char_p, [_ST]),
@@ -356,6 +358,19 @@ def block_attn_bwd_dq_convert(plan: Plan, dq_acc, dq, stream=None) -> None:
     _need(dq, torch.bfloat16, (hq, T, D), "dq")
     _check(lib().fcp_block_attn_bwd_dq_convert(plan.handle, _ptr(dq_acc), hq, D, _ptr(dq), _stream(stream)),
            "fcp_block_attn_bwd_dq_convert")
+
+
+def reshuffle(plan: Plan, d_plan, src, dst, to_workers: bool = True, stream=None) -> None:
+    """Permute the token rows of src [H, T, ...] between the user's and the workers' layout
+    into dst (fcp_reshuffle)."""
+    if src.shape != dst.shape or src.dtype != dst.dtype:
+        raise ValueError("src and dst must have the same shape and dtype")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src and dst must be contiguous")
+    heads = src.shape[0]
+    row_bytes = src[0, 0].numel() * src.element_size() if src.shape[1] else 16
+    _check(lib().fcp_reshuffle(plan.handle, _ptr(d_plan), _ptr(src), _ptr(dst), heads, row_bytes,
+                               0 if to_workers else 1, _stream(stream)), "fcp_reshuffle")
 
 
 def device_error(d_plan, stream=None) -> int:

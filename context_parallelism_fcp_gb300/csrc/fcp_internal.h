@@ -50,7 +50,7 @@ static_assert(sizeof(DevHeader) == 256, "header is one 256-byte line");
 
 // Byte offsets of the arrays in the device image and their lengths.
 struct DevLayout {
-  size_t items = 0, runs = 0, qsegs = 0, tok2part = 0, fwd_units = 0, kvsegs = 0, kv_items = 0,
+  size_t items = 0, runs = 0, qsegs = 0, tok2part = 0, worker_order = 0, fwd_units = 0, kvsegs = 0, kv_items = 0,
          bwd_units = 0, total = 0;
   int32_t n_qsegs = 0, n_fwd_units = 0, n_kvsegs = 0, n_kv_items = 0, n_bwd_units = 0;
   int32_t max_runs_per_qseg = 0;

@@ -284,6 +284,30 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Row permutation between the user's and the workers' token layouts, 16 bytes per thread
+// per iteration: unit u of a head covers chunk (u % chunks) of worker-layout row
+// (u / chunks); writes (gather) or reads (scatter) of consecutive threads are contiguous.
+template <bool kToWorkers>
+__global__ void __launch_bounds__(256)
+    reshuffle_kernel(const int* __restrict__ order, const uint4* __restrict__ src, uint4* __restrict__ dst,
+                     long long T, int chunks, long long total) {
+  const long long per_head = T * chunks;
+  for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
+       u += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long h = u / per_head;
+    const long long r = u - h * per_head;
+    const long long i = r / chunks;
+    const int c = static_cast<int>(r - i * chunks);
+    const long long user = order[i];
+    const long long wi = (h * T + i) * chunks + c;
+    const long long ui = (h * T + user) * chunks + c;
+    if (kToWorkers)
+      dst[wi] = __ldg(src + ui);
+    else
+      dst[ui] = __ldg(src + wi);
+  }
+}
+
 }  // namespace
 
 fcp_status launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale, cudaStream_t s) {
@@ -364,6 +388,33 @@ fcp_status fcp_block_attn_merge(const fcp_plan* plan, const void* d_plan, const 
   else
     merge_kernel<64><<<grid, 32 * kRowWarps, 0, s>>>(tok2, part_o, part_lse, plan->partial_rows, T, out, lse);
   FCP_CUDA_TRY(cudaGetLastError(), "merge launch");
+  return FCP_OK;
+}
+
+fcp_status fcp_reshuffle(const fcp_plan* plan, const void* d_plan, const void* src, void* dst, int32_t heads,
+                         int32_t row_bytes, int32_t direction, void* stream) {
+  if (plan == nullptr || d_plan == nullptr || heads <= 0 || row_bytes <= 0 || (row_bytes & 15) != 0 ||
+      (direction != 0 && direction != 1))
+    return FCP_ERR_INVALID;
+  if (!plan->distributed) return FCP_ERR_STATE;
+  const int64_t T = plan->total_tokens;
+  if (T == 0) return FCP_OK;
+  if (!src || !dst || src == dst || !aligned16(src) || !aligned16(dst)) return FCP_ERR_INVALID;
+  const int chunks = row_bytes / 16;
+  const long long total = static_cast<long long>(heads) * T * chunks;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long want = (total + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(want < 16LL * sms ? want : 16LL * sms);
+  const auto* order = dev_array<int>(d_plan, plan->layout.worker_order);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (direction == 0)
+    reshuffle_kernel<true><<<grid, 256, 0, s>>>(order, static_cast<const uint4*>(src), static_cast<uint4*>(dst), T,
+                                               chunks, total);
+  else
+    reshuffle_kernel<false><<<grid, 256, 0, s>>>(order, static_cast<const uint4*>(src), static_cast<uint4*>(dst), T,
+                                                chunks, total);
+  FCP_CUDA_TRY(cudaGetLastError(), "reshuffle launch");
   return FCP_OK;
 }
 

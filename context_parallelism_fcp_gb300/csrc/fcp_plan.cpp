@@ -157,6 +157,17 @@ bool build_image(fcp_plan* p) {
   bwd_units.reserve(bu.size());
   for (auto& x : bu) bwd_units.push_back(x.second);
 
+  // workers' token layout: worker w's blocks in ascending id, their segments in order
+  std::vector<int32_t> worker_order;
+  worker_order.reserve(static_cast<size_t>(p->total_tokens));
+  for (int32_t w = 0; w < p->n_workers; ++w)
+    for (const fcp_block& B : p->blocks) {
+      if (B.worker != w) continue;
+      for (int32_t si = B.first_seg; si < B.first_seg + B.n_segs; ++si)
+        for (int32_t t = 0; t < p->segs[si].len; ++t) worker_order.push_back(p->segs[si].tok0 + t);
+    }
+  if (static_cast<int64_t>(worker_order.size()) != p->total_tokens) return false;
+
   DevLayout L;
   size_t off = sizeof(DevHeader);
   L.items = off;
@@ -167,6 +178,8 @@ bool build_image(fcp_plan* p) {
   off = align256(off + qsegs.size() * sizeof(QSeg));
   L.tok2part = off;
   off = align256(off + tok2part.size() * sizeof(TokPart));
+  L.worker_order = off;
+  off = align256(off + worker_order.size() * sizeof(int32_t));
   L.fwd_units = off;
   off = align256(off + fwd_units.size() * sizeof(FwdUnit));
   L.kvsegs = off;
@@ -190,6 +203,7 @@ bool build_image(fcp_plan* p) {
   put(p->image, L.runs, p->runs);
   put(p->image, L.qsegs, qsegs);
   put(p->image, L.tok2part, tok2part);
+  put(p->image, L.worker_order, worker_order);
   put(p->image, L.fwd_units, fwd_units);
   put(p->image, L.kvsegs, kvsegs);
   put(p->image, L.kv_items, kv_items);

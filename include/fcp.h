@@ -236,6 +236,18 @@ fcp_status fcp_block_attn_bwd_static_scratch(const fcp_plan* plan, const void* d
                                              const float* lse, int32_t hq, int32_t hkv, int32_t head_dim, void* dq,
                                              void* dk, void* dv, void* stream);
 
+/* Transparent reshuffle (Section 4.3): the two all-to-alls around attention become, on one
+ * GPU, a permutation of token rows between the user's layout (tokens in input order) and
+ * the workers' layout (worker 0's blocks in ascending id -- each block's segments in order
+ * -- then worker 1's, ...). For every head h < heads and row i < T:
+ *   direction 0 (to workers):  dst[h, i, :] = src[h, user_token(i), :]
+ *   direction 1 (to users):    dst[h, user_token(i), :] = src[h, i, :]
+ * where user_token(i) is the input position of worker-layout row i. src and dst are
+ * distinct device buffers of heads * T * row_bytes bytes; row_bytes is a multiple of 16
+ * (e.g. 256 for bf16 rows of D = 128). Errors: FCP_ERR_INVALID, FCP_ERR_STATE, FCP_ERR_CUDA. */
+fcp_status fcp_reshuffle(const fcp_plan* plan, const void* d_plan, const void* src, void* dst, int32_t heads,
+                         int32_t row_bytes, int32_t direction, void* stream);
+
 /* Synchronise `stream`, copy the device plan's error word to *code (0 = none; else the
  * kernel and wait that gave up) and clear it. Returns FCP_ERR_DEVICE if it was set. */
 fcp_status fcp_device_error(const void* d_plan, int32_t* code, void* stream);

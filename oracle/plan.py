@@ -256,3 +256,17 @@ def stages_are_matchings(edges: Sequence[tuple], stage: Sequence[int], n_stages:
         sent.add((s, e[1]))
         got.add((s, e[2]))
     return True
+
+
+def worker_order(part: Dict[str, list], dist: Dict[str, list], n_workers: int) -> List[int]:
+    """The workers' token layout of the transparent reshuffle (Section 4.3): position i holds
+    the input token of worker 0's blocks (ascending id, segments in order), then worker 1's..."""
+    order: List[int] = []
+    for w in range(n_workers):
+        for b, blk in enumerate(part["blocks"]):
+            if dist["worker_of_block"][b] != w:
+                continue
+            for si in range(blk[0], blk[0] + blk[1]):
+                _, _, ln, tok0 = part["segs"][si]
+                order.extend(range(tok0, tok0 + ln))
+    return order

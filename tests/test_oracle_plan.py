@@ -270,3 +270,29 @@ def test_every_remote_pair_has_a_transfer():
         for (w, qb, kb, *_rest) in dist["items"]:
             if dist["worker_of_block"][kb] != w:
                 assert (kb, w) in have
+
+
+def test_worker_order_hand_worked():
+    """8-token causal sequence, 2-token blocks, 2 workers: w0 holds blocks 0 and 3 (tokens
+    0,1 and 6,7), w1 holds blocks 1 and 2 (tokens 2..5)."""
+    part = P.partition([8], 2, True)
+    dist = P.distribute(part, 2)
+    assert P.worker_order(part, dist, 2) == [0, 1, 6, 7, 2, 3, 4, 5]
+
+
+@pytest.mark.parametrize("seqlens,b,causal,n", _tiny_cases())
+def test_worker_order_is_a_permutation(seqlens, b, causal, n):
+    part = P.partition(seqlens, b, causal)
+    dist = P.distribute(part, n)
+    order = P.worker_order(part, dist, n)
+    assert sorted(order) == list(range(sum(seqlens)))
+    # contiguous per worker, in token counts equal to the worker's tokens
+    sizes = dist["tokens"]
+    starts = [sum(sizes[:w]) for w in range(n)]
+    for w in range(n):
+        chunk = order[starts[w]:starts[w] + sizes[w]]
+        for t in chunk:
+            seg_block = [bi for bi, blk in enumerate(part["blocks"])
+                         for si in range(blk[0], blk[0] + blk[1])
+                         if part["segs"][si][3] <= t < part["segs"][si][3] + part["segs"][si][2]]
+            assert dist["worker_of_block"][seg_block[0]] == w
