@@ -145,10 +145,11 @@ class ClockSampler:
 class Step:
     """Buffers and launches of one batch; run() enqueues one whole step on `stream`."""
 
-    def __init__(self, fcp, torch, w, coalesce, device, stream):
+    def __init__(self, fcp, torch, w, coalesce, device, stream, planner="fcp"):
         import workloads as W
 
         self.fcp, self.torch, self.w, self.c, self.dev, self.stream = fcp, torch, w, coalesce, device, stream
+        self.planner = planner
         self.q, self.k, self.v = W.make_qkv(w, device=device)
         self.do = W.make_dout(w, device=device)
         plan = self.make_plan()
@@ -177,7 +178,10 @@ class Step:
 
     def make_plan(self):
         w = self.w
-        plan = self.fcp.Plan(w.seqlens, w.block_size, w.causal).distribute(w.n_workers, w.token_cap)
+        if self.planner == "ring":
+            plan = self.fcp.Plan.ring(w.seqlens, w.n_workers, w.causal)
+        else:
+            plan = self.fcp.Plan(w.seqlens, w.block_size, w.causal).distribute(w.n_workers, w.token_cap)
         if self.c != 1:
             plan.coalesce(self.c)
         return plan
@@ -383,9 +387,12 @@ def bench_fcp(args):
 
     result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
     if not args.no_sweep:
+        result["fcp_vs_ring"] = planner_compare(torch, fcp, W, dev, stream, flush, sustained)
+    if not args.no_sweep:
         result["sweep"] = sweep(torch, fcp, W, args, dev, stream, flush, sustained)
     if rank == 0:
         result["solver"] = solver_report(fcp, W)
+        result["balance"] = balance_report(W)
     if cpu is not None:
         result["cpu_baseline"] = cpu
     if rank == 0:
@@ -474,6 +481,26 @@ def reshuffle_bench(torch, fcp, step, stream, flush, pk):
             "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": nbytes, "kernel": "reshuffle_kernel"}
 
 
+def planner_compare(torch, fcp, W, dev, stream, flush, sustained):
+    """Attention fwd+bwd TFLOP/s of the causal mixed batch (65536 tokens, 16 workers) under
+    FCP's plan (4K blocks, LPT) and under the ring baseline's (2N blocks per sequence), with
+    one partial per pair (c = 1) and with coalescing (c = 16)."""
+    w = W.causal_mixed()
+    out = []
+    for planner in ("fcp", "ring"):
+        for c in (1, 16):
+            st = Step(fcp, torch, w, c, dev, stream, planner=planner)
+            times = timed_steps(torch, st, 3, 2, flush)
+            ms = statistics.mean(t["total"] for t in times)
+            tf = (st.fwd_flops + st.bwd_flops) / (ms * 1e-3) / 1e12
+            v = st.plan.view()
+            out.append({"planner": planner, "coalesce": c, "blocks": v["n_blocks"], "items": v["n_items"],
+                        "ms": round(ms, 3), "fwd_bwd_tflops": round(tf, 1), "frac_of_peak": round(tf / sustained, 4)})
+            del st
+            torch.cuda.empty_cache()
+    return out
+
+
 def solver_report(fcp, W):
     """Host time of the congestion-free solver on the pages' cluster setting (256 workers,
     32K tokens each, 4K blocks) and on the benchmark's own plan."""
@@ -490,6 +517,18 @@ def solver_report(fcp, W):
                      "stages": res["n_stages"], "plan_ms": round((t1 - t0) * 1e3, 2),
                      "solve_ms": round((t2 - t1) * 1e3, 2),
                      "imbalance": round((mx - sum(loads) / len(loads)) / mx, 6) if mx else 0.0}
+    return out
+
+
+def balance_report(W):
+    """FCP vs the ring baseline on the pages' kind of batches (plan level, host only). The
+    ring plan of a 256-worker batch has hundreds of thousands of blocks and tens of millions
+    of work items, so the cluster comparison runs at 32 workers x 32K tokens."""
+    from context_parallelism_fcp_gb300 import balance
+
+    out = {}
+    for w in (W.full_mask(), W.causal_mixed(), W.cluster_batch(n_workers=32)):
+        out[w.name] = balance.compare(w.seqlens, w.block_size, w.n_workers, w.causal, w.token_cap)
     return out
 
 

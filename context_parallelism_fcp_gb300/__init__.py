@@ -106,6 +106,7 @@ _ST = ctypes.c_int
 _SIGNATURES = {
     "fcp_partition": (_ST, [ctypes.POINTER(_I32), _I32, _I32, _I32, ctypes.POINTER(_P)]),
     "fcp_distribute": (_ST, [_P, _I32, _I64]),
+    "fcp_partition_ring": (_ST, [ctypes.POINTER(_I32), _I32, _I32, _I32, ctypes.POINTER(_P)]),
     "fcp_coalesce": (_ST, [_P, _I32]),
     "fcp_plan_query": (_ST, [_P, ctypes.POINTER(_View)]),
     "fcp_solve_stages": (_ST, [_P]),
@@ -186,6 +187,22 @@ class Plan:
         self.seqlens = [int(x) for x in seqlens]
         self.block_size = int(block_size)
         self.causal = bool(causal)
+
+    @classmethod
+    def ring(cls, seqlens: Sequence[int], n_workers: int, causal: bool) -> "Plan":
+        """The ring-attention baseline plan: 2N equal blocks per sequence, worker w holding
+        blocks w and 2N-1-w (fcp_partition_ring); already distributed."""
+        self = cls.__new__(cls)
+        L = lib()
+        arr = (_I32 * len(seqlens))(*[int(x) for x in seqlens])
+        h = _P()
+        _check(L.fcp_partition_ring(arr, len(seqlens), int(n_workers), 1 if causal else 0, ctypes.byref(h)),
+               "fcp_partition_ring")
+        self._h = h
+        self.seqlens = [int(x) for x in seqlens]
+        self.block_size = None
+        self.causal = bool(causal)
+        return self
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -391,11 +408,25 @@ class FcpAttention:
                  backward: bool = True):
         import torch
 
-        self.plan = Plan(seqlens, block_size, causal).distribute(n_workers, token_cap)
+        plan = Plan(seqlens, block_size, causal).distribute(n_workers, token_cap)
         if coalesce != 1:
-            self.plan.coalesce(coalesce)
+            plan.coalesce(coalesce)
+        self._setup(plan, hq, hkv, head_dim, device, backward)
+
+    @classmethod
+    def from_plan(cls, plan: "Plan", hq: int, hkv: int, head_dim: int, device="cuda",
+                  backward: bool = True) -> "FcpAttention":
+        """Wrap an already distributed plan (e.g. Plan.ring(...))."""
+        self = cls.__new__(cls)
+        self._setup(plan, hq, hkv, head_dim, device, backward)
+        return self
+
+    def _setup(self, plan, hq, hkv, head_dim, device, backward):
+        import torch
+
+        self.plan = plan
         self.hq, self.hkv, self.head_dim = hq, hkv, head_dim
-        self.T = sum(int(x) for x in seqlens)
+        self.T = sum(int(x) for x in plan.seqlens)
         self.device = torch.device(device)
         nbytes = self.plan.device_bytes()
         self.d_plan = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)

@@ -212,6 +212,67 @@ bool build_image(fcp_plan* p) {
   return true;
 }
 
+// Loads, tokens, work list, runs and device image of a plan whose blocks have owners.
+// Work list: per worker, per owned block (ascending id), per segment; an unpacked causal
+// block j of a sequence pairs with KV blocks 0..j of it (j: CAUSAL_DIAG), a full-mask block
+// with every block of its sequence, a packed segment with itself.
+fcp_status finish_distribution(fcp_plan* p, const std::vector<int32_t>& owner, int32_t n_workers, int64_t cap) {
+  const int32_t K = static_cast<int32_t>(p->blocks.size());
+  std::vector<int64_t> load(static_cast<size_t>(n_workers), 0), tokens(static_cast<size_t>(n_workers), 0);
+  for (int32_t b = 0; b < K; ++b) {
+    load[owner[b]] += p->blocks[b].cost;
+    tokens[owner[b]] += p->blocks[b].tokens;
+  }
+
+  // blocks of each unpacked sequence, in position order (they were created in order)
+  std::vector<std::vector<int32_t>> seq_blocks(p->seqlens.size());
+  for (int32_t b = 0; b < K; ++b)
+    if (p->blocks[b].seq >= 0) seq_blocks[p->blocks[b].seq].push_back(b);
+
+  std::vector<std::vector<int32_t>> owned(static_cast<size_t>(n_workers));
+  for (int32_t b = 0; b < K; ++b) owned[owner[b]].push_back(b);
+
+  const bool c = p->causal != 0;
+  p->items.clear();
+  for (int32_t w = 0; w < n_workers; ++w) {
+    for (int32_t qb : owned[w]) {
+      const fcp_block& B = p->blocks[qb];
+      for (int32_t si = B.first_seg; si < B.first_seg + B.n_segs; ++si) {
+        const fcp_segment& qs = p->segs[si];
+        if (B.seq < 0) {
+          fcp_item it{w, qb, qb, qs.tok0, qs.len, qs.tok0, qs.len,
+                      c ? FCP_MASK_CAUSAL_DIAG : FCP_MASK_FULL, -1, 0};
+          p->items.push_back(it);
+          continue;
+        }
+        const auto& kvs = seq_blocks[B.seq];
+        const size_t nkv = c ? static_cast<size_t>(B.seq_block_idx) + 1 : kvs.size();
+        for (size_t x = 0; x < nkv; ++x) {
+          const int32_t kb = kvs[x];
+          const fcp_segment& ks = p->segs[p->blocks[kb].first_seg];
+          fcp_item it{w, qb, kb, qs.tok0, qs.len, ks.tok0, ks.len,
+                      (c && kb == qb) ? FCP_MASK_CAUSAL_DIAG : FCP_MASK_FULL, -1, 0};
+          p->items.push_back(it);
+        }
+      }
+    }
+  }
+  p->n_workers = n_workers;
+  p->token_cap = cap;
+  p->load = std::move(load);
+  p->tokens = std::move(tokens);
+  p->distributed = true;
+  p->solved = false;
+  p->transfers.clear();
+  p->n_stages = 0;
+  build_runs(p, 1);
+  if (!build_image(p)) {
+    p->distributed = false;
+    return FCP_ERR_STATE;
+  }
+  return FCP_OK;
+}
+
 }  // namespace
 
 void set_last_error(const std::string& msg) { g_last_error = msg; }
@@ -347,53 +408,70 @@ fcp_status fcp_distribute(fcp_plan* p, int32_t n_workers, int64_t token_cap) {
     by_load.insert({load[chosen], chosen});
   }
   for (int32_t b = 0; b < K; ++b) p->blocks[b].worker = owner[b];
+  return finish_distribution(p, owner, n_workers, cap);
+}
 
-  // blocks of each unpacked sequence, in position order (they were created in order)
-  std::vector<std::vector<int32_t>> seq_blocks(p->seqlens.size());
-  for (int32_t b = 0; b < K; ++b)
-    if (p->blocks[b].seq >= 0) seq_blocks[p->blocks[b].seq].push_back(b);
-
-  std::vector<std::vector<int32_t>> owned(static_cast<size_t>(n_workers));
-  for (int32_t b = 0; b < K; ++b) owned[owner[b]].push_back(b);
-
+fcp_status fcp_partition_ring(const int32_t* seqlens, int32_t n_seqs, int32_t n_workers, int32_t causal,
+                              fcp_plan** out) {
+  if (out == nullptr || n_seqs < 0 || n_workers <= 0 || (n_seqs > 0 && seqlens == nullptr)) return FCP_ERR_INVALID;
+  *out = nullptr;
+  int64_t T = 0;
+  for (int32_t i = 0; i < n_seqs; ++i) {
+    if (seqlens[i] < 0) return FCP_ERR_INVALID;
+    T += seqlens[i];
+  }
+  if (T >= (int64_t(1) << 31)) return FCP_ERR_INVALID;
+  fcp_plan* p = new fcp_plan();
+  p->seqlens.assign(seqlens, seqlens + n_seqs);
+  p->causal = causal ? 1 : 0;
+  p->total_tokens = T;
   const bool c = p->causal != 0;
-  p->items.clear();
-  for (int32_t w = 0; w < n_workers; ++w) {
-    for (int32_t qb : owned[w]) {
-      const fcp_block& B = p->blocks[qb];
-      for (int32_t si = B.first_seg; si < B.first_seg + B.n_segs; ++si) {
-        const fcp_segment& qs = p->segs[si];
-        if (B.seq < 0) {
-          fcp_item it{w, qb, qb, qs.tok0, qs.len, qs.tok0, qs.len,
-                      c ? FCP_MASK_CAUSAL_DIAG : FCP_MASK_FULL, -1, 0};
-          p->items.push_back(it);
-          continue;
-        }
-        const auto& kvs = seq_blocks[B.seq];
-        const size_t nkv = c ? static_cast<size_t>(B.seq_block_idx) + 1 : kvs.size();
-        for (size_t x = 0; x < nkv; ++x) {
-          const int32_t kb = kvs[x];
-          const fcp_segment& ks = p->segs[p->blocks[kb].first_seg];
-          fcp_item it{w, qb, kb, qs.tok0, qs.len, ks.tok0, ks.len,
-                      (c && kb == qb) ? FCP_MASK_CAUSAL_DIAG : FCP_MASK_FULL, -1, 0};
-          p->items.push_back(it);
-        }
-      }
+  const int64_t two_n = 2 * int64_t(n_workers);
+  std::vector<int32_t> owner;
+  int32_t max_len = 1;
+  int64_t acc = 0;
+  for (int32_t i = 0; i < n_seqs; ++i) {
+    const int64_t L = seqlens[i];
+    const int32_t tok0 = static_cast<int32_t>(acc);
+    acc += L;
+    p->total_pairs += c ? L * (L + 1) / 2 : L * L;
+    std::vector<int32_t> grid(static_cast<size_t>(two_n), -1);
+    const int32_t first = static_cast<int32_t>(p->blocks.size());
+    int32_t dense = 0;
+    for (int64_t j = 0; j < two_n; ++j) {
+      const int64_t a = j * L / two_n, e = (j + 1) * L / two_n;
+      if (e == a) continue;
+      fcp_block b{};
+      b.first_seg = static_cast<int32_t>(p->segs.size());
+      b.n_segs = 1;
+      b.tokens = static_cast<int32_t>(e - a);
+      b.seq = i;
+      b.seq_block_idx = dense++;
+      b.worker = static_cast<int32_t>(j < n_workers ? j : two_n - 1 - j);
+      b.cost = segment_cost(a, e - a, L, c);
+      grid[static_cast<size_t>(j)] = static_cast<int32_t>(p->blocks.size());
+      owner.push_back(b.worker);
+      max_len = std::max(max_len, b.tokens);
+      p->blocks.push_back(b);
+      p->segs.push_back(fcp_segment{i, static_cast<int32_t>(a), static_cast<int32_t>(e - a), tok0 + static_cast<int32_t>(a)});
     }
+    for (int64_t j = 0; j < two_n; ++j) {
+      const int32_t id = grid[static_cast<size_t>(j)];
+      if (id < 0) continue;
+      p->blocks[id].seq_nblocks = dense;
+      const int32_t partner = grid[static_cast<size_t>(two_n - 1 - j)];
+      p->blocks[id].zz_partner = (c && partner >= 0 && partner != id) ? partner : -1;
+    }
+    (void)first;
   }
-  p->n_workers = n_workers;
-  p->token_cap = cap;
-  p->load = std::move(load);
-  p->tokens = std::move(tokens);
-  p->distributed = true;
-  p->solved = false;
-  p->transfers.clear();
-  p->n_stages = 0;
-  build_runs(p, 1);
-  if (!build_image(p)) {
-    p->distributed = false;
-    return FCP_ERR_STATE;
+  p->block_size = max_len;
+  fcp_status st = finish_distribution(p, owner, n_workers, 0);
+  if (st != FCP_OK) {
+    delete p;
+    return st;
   }
+  p->token_cap = *std::max_element(p->tokens.begin(), p->tokens.end());
+  *out = p;
   return FCP_OK;
 }
 

@@ -126,6 +126,17 @@ fcp_status fcp_partition(const int32_t* seqlens, int32_t n_seqs, int32_t block_s
  * (null plan, n_workers <= 0), FCP_ERR_CAPACITY (the plan is left undistributed). */
 fcp_status fcp_distribute(fcp_plan* plan, int32_t n_workers, int64_t token_cap);
 
+/* The ring-attention baseline the pages compare against (Section 3.4, "Balance-optimized",
+ * Figure 5a; Zig-Zag of Figure 4), as a distributed plan: every sequence of length L is cut
+ * into 2N equal blocks, block j covering [j*L/(2N), (j+1)*L/(2N)) (integer division; empty
+ * blocks are skipped, so a sequence shorter than 2N tokens has fewer blocks), and worker w
+ * takes blocks w and 2N-1-w of every sequence. Block ids follow the sequences in input order;
+ * the work list, runs, device image and token_cap (= the largest worker's tokens) are built
+ * as in fcp_distribute, so every other call (fcp_coalesce, fcp_solve_stages, the kernels)
+ * accepts the result. Errors: FCP_ERR_INVALID as fcp_partition, or n_workers <= 0. */
+fcp_status fcp_partition_ring(const int32_t* seqlens, int32_t n_seqs, int32_t n_workers, int32_t causal,
+                              fcp_plan** out);
+
 /* Bottom-up coalescing (Section 4.2): rebuild runs so that up to `degree` consecutive
  * items of one worker over the same query range share one partial result. degree = 1
  * gives one partial per (Q-block, KV-block) pair. Errors: FCP_ERR_INVALID (degree <= 0),

@@ -155,30 +155,10 @@ def distribute(part: Dict[str, list], n_workers: int, token_cap: Optional[int] =
         load[best] += blocks[b][7]
         tokens[best] += need
 
-    # blocks of each unpacked sequence, by position
-    seq_blocks: Dict[int, List[int]] = {}
-    for b, blk in enumerate(blocks):
-        if blk[3] >= 0:
-            seq_blocks.setdefault(blk[3], []).append(b)
+    out = distribute_fixed(part, owner, n_workers)
+    out["cap"] = cap
+    return out
 
-    causal = part["causal"]
-    items: List[tuple] = []
-    for w in range(n_workers):
-        for qb in range(K):
-            if owner[qb] != w:
-                continue
-            first, nseg, _, seq, j, _, _, _ = blocks[qb]
-            for si in range(first, first + nseg):
-                _, _, qlen, qtok = segs[si]
-                if seq < 0:  # packed segment: attends to itself only
-                    items.append((w, qb, qb, qtok, qlen, qtok, qlen, CAUSAL_DIAG if causal else FULL))
-                    continue
-                kv_list = seq_blocks[seq][: j + 1] if causal else seq_blocks[seq]
-                for kb in kv_list:
-                    kseg = segs[blocks[kb][0]]
-                    mask = CAUSAL_DIAG if (causal and kb == qb) else FULL
-                    items.append((w, qb, kb, qtok, qlen, kseg[3], kseg[2], mask))
-    return {"worker_of_block": owner, "load": load, "tokens": tokens, "cap": cap, "items": items}
 
 
 def coalesce(items: Sequence[tuple], degree: int) -> List[tuple]:
@@ -270,3 +250,70 @@ def worker_order(part: Dict[str, list], dist: Dict[str, list], n_workers: int) -
                 _, _, ln, tok0 = part["segs"][si]
                 order.extend(range(tok0, tok0 + ln))
     return order
+
+
+def partition_ring(seqlens: Sequence[int], n_workers: int, causal: bool) -> Dict[str, list]:
+    """Ring attention's sharding and assignment (Section 3.4 "Balance-optimized", Figure 5a,
+    with the Zig-Zag order of Figure 4): each sequence of length L is cut into 2N equal
+    blocks, block j covering [j*L // 2N, (j+1)*L // 2N); empty blocks are dropped; worker w
+    takes blocks w and 2N-1-w. Returns the partition (same tuples as `partition`) and the
+    owner of every block."""
+    two_n = 2 * n_workers
+    blocks: List[tuple] = []
+    segs: List[tuple] = []
+    owner: List[int] = []
+    tok0 = 0
+    for i, L in enumerate(seqlens):
+        grid = {}
+        made = []
+        for j in range(two_n):
+            a, e = j * L // two_n, (j + 1) * L // two_n
+            if e == a:
+                continue
+            grid[j] = len(blocks)
+            made.append(j)
+            blocks.append([len(segs), 1, e - a, i, len(made) - 1, 0, -1, segment_cost(a, e - a, L, causal)])
+            segs.append((i, a, e - a, tok0 + a))
+            owner.append(j if j < n_workers else two_n - 1 - j)
+        for j in made:
+            b = blocks[grid[j]]
+            b[5] = len(made)
+            partner = grid.get(two_n - 1 - j, -1)
+            b[6] = partner if (causal and partner >= 0 and partner != grid[j]) else -1
+        tok0 += L
+    return {"blocks": [tuple(b) for b in blocks], "segs": segs, "seqlens": list(seqlens),
+            "block_size": max([b[2] for b in blocks], default=1), "causal": causal, "owner": owner}
+
+
+def distribute_fixed(part: Dict[str, list], owner: Sequence[int], n_workers: int) -> Dict[str, list]:
+    """Loads, tokens and the work list of a partition whose owners are given (same work-list
+    rule as `distribute`)."""
+    blocks, segs = part["blocks"], part["segs"]
+    load = [0] * n_workers
+    tokens = [0] * n_workers
+    for b, blk in enumerate(blocks):
+        load[owner[b]] += blk[7]
+        tokens[owner[b]] += blk[2]
+    seq_blocks: Dict[int, List[int]] = {}
+    for b, blk in enumerate(blocks):
+        if blk[3] >= 0:
+            seq_blocks.setdefault(blk[3], []).append(b)
+    causal = part["causal"]
+    items: List[tuple] = []
+    for w in range(n_workers):
+        for qb in range(len(blocks)):
+            if owner[qb] != w:
+                continue
+            first, nseg, _, seq, j, _, _, _ = blocks[qb]
+            for si in range(first, first + nseg):
+                _, _, qlen, qtok = segs[si]
+                if seq < 0:
+                    items.append((w, qb, qb, qtok, qlen, qtok, qlen, CAUSAL_DIAG if causal else FULL))
+                    continue
+                kv_list = seq_blocks[seq][: j + 1] if causal else seq_blocks[seq]
+                for kb in kv_list:
+                    kseg = segs[blocks[kb][0]]
+                    mask = CAUSAL_DIAG if (causal and kb == qb) else FULL
+                    items.append((w, qb, kb, qtok, qlen, kseg[3], kseg[2], mask))
+    return {"worker_of_block": list(owner), "load": load, "tokens": tokens, "cap": max(tokens, default=0),
+            "items": items}

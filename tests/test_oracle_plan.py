@@ -296,3 +296,30 @@ def test_worker_order_is_a_permutation(seqlens, b, causal, n):
                          for si in range(blk[0], blk[0] + blk[1])
                          if part["segs"][si][3] <= t < part["segs"][si][3] + part["segs"][si][2]]
             assert dist["worker_of_block"][seg_block[0]] == w
+
+
+@pytest.mark.parametrize("n,b", [(1, 4), (2, 2), (4, 8), (8, 512)])
+def test_ring_equals_zigzag_plan_on_one_causal_sequence(n, b):
+    """On one causal sequence of 2N*b tokens, ring's 2N equal blocks with worker w holding
+    blocks w and 2N-1-w is the same plan as fixed blocks of b tokens with LPT (Zig-Zag)."""
+    ring = P.partition_ring([2 * n * b], n, True)
+    fcp = P.partition([2 * n * b], b, True)
+    assert ring["blocks"] == fcp["blocks"] and ring["segs"] == fcp["segs"]
+    assert ring["owner"] == P.distribute(fcp, n)["worker_of_block"]
+
+
+def test_ring_short_and_uneven_sequences():
+    part = P.partition_ring([3, 10], 2, True)  # 2N = 4
+    # L=3: j=0 empty, then [0,1), [1,2), [2,3); L=10: [0,2), [2,5), [5,7), [7,10)
+    assert [s[1:3] for s in part["segs"]] == [(0, 1), (1, 1), (2, 1), (0, 2), (2, 3), (5, 2), (7, 3)]
+    assert part["owner"] == [1, 1, 0, 0, 1, 1, 0]
+    dist = P.distribute_fixed(part, part["owner"], 2)
+    assert sum(dist["load"]) == 3 * 4 // 2 + 10 * 11 // 2
+    assert dist["tokens"] == [1 + 2 + 3, 2 + 3 + 2]
+
+
+@pytest.mark.parametrize("n", [2, 3, 8])
+def test_ring_compute_is_balanced_when_divisible(n):
+    part = P.partition_ring([2 * n * 5, 2 * n * 7], n, True)
+    dist = P.distribute_fixed(part, part["owner"], n)
+    assert len(set(dist["load"])) == 1 and len(set(dist["tokens"])) == 1

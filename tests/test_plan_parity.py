@@ -155,3 +155,27 @@ def test_solver_state_errors(fcp):
     p.distribute(1)  # one worker: nothing moves
     res = p.solve()
     assert res["n_stages"] == 0 and len(res["transfers"]) == 0
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_ring_plan_bit_exact(fcp, seed):
+    r = random.Random(2000 + seed)
+    n = r.randint(1, 9)
+    seqlens = [r.choice([0, r.randint(1, 3 * n), r.randint(1, 500)]) for _ in range(r.randint(1, 8))]
+    causal = r.random() < 0.6
+    part = P.partition_ring(seqlens, n, causal)
+    dist = P.distribute_fixed(part, part["owner"], n)
+    plan = fcp.Plan.ring(seqlens, n, causal)
+    v = plan.view()
+    assert v["n_blocks"] == len(part["blocks"])
+    if part["blocks"]:
+        assert np.array_equal(v["blocks"], np.array(part["blocks"], dtype=np.int64))
+        assert np.array_equal(v["segs"], np.array(part["segs"], dtype=np.int64))
+        assert list(v["worker_of_block"]) == part["owner"]
+    assert list(v["load"]) == dist["load"] and list(v["tokens"]) == dist["tokens"]
+    if dist["items"]:
+        assert np.array_equal(v["items"], np.array(dist["items"], dtype=np.int64))
+    assert v["token_cap"] == (max(dist["tokens"]) if dist["tokens"] else 0)
+    res = plan.solve()
+    edges = P.transfers(part, dist)
+    assert res["n_stages"] == P.max_degree(edges, n)
