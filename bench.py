@@ -145,11 +145,13 @@ class ClockSampler:
 class Step:
     """Buffers and launches of one batch; run() enqueues one whole step on `stream`."""
 
-    def __init__(self, fcp, torch, w, coalesce, device, stream, planner="fcp"):
+    def __init__(self, fcp, torch, w, coalesce, device, stream, planner="fcp", pipeline=None, replan=True):
         import workloads as W
 
         self.fcp, self.torch, self.w, self.c, self.dev, self.stream = fcp, torch, w, coalesce, device, stream
         self.planner = planner
+        self.pipeline = pipeline  # coalesce degree of the block-level pipeline, or None
+        self.replan = replan  # rebuild the plan inside each step (host work in the timed region)
         self.q, self.k, self.v = W.make_qkv(w, device=device)
         self.do = W.make_dout(w, device=device)
         plan = self.make_plan()
@@ -174,7 +176,10 @@ class Step:
         for r in v["runs"]:
             per_row_parts[(int(r[2]), int(r[3]))] = per_row_parts.get((int(r[2]), int(r[3])), 0) + 1
         self.merge_bytes = sum(n * qlen * (4 * D + 4) + qlen * (2 * D + 4) for (_, qlen), n in per_row_parts.items()) * hq
-        self.n_launches = 5
+        self.n_stages = int(v["n_exec_stages"])
+        self.n_launches = 4 + self.n_stages
+        if not replan:
+            plan.upload(self.d_plan, stream)
 
     def make_plan(self):
         w = self.w
@@ -182,7 +187,9 @@ class Step:
             plan = self.fcp.Plan.ring(w.seqlens, w.n_workers, w.causal)
         else:
             plan = self.fcp.Plan(w.seqlens, w.block_size, w.causal).distribute(w.n_workers, w.token_cap)
-        if self.c != 1:
+        if self.pipeline is not None:
+            plan.schedule(self.pipeline)
+        elif self.c != 1:
             plan.coalesce(self.c)
         return plan
 
@@ -191,10 +198,16 @@ class Step:
         f, s = self.fcp, self.stream
         rec = (lambda i: ev[i].record(s)) if ev is not None else (lambda i: None)
         rec(0)
-        plan = self.make_plan()  # host: partition + LPT distribute + coalesce
-        plan.upload(self.d_plan, s)
-        self.plan = plan
-        f.block_attn_fwd(plan, self.d_plan, self.q, self.k, self.v, self.part_o, self.part_lse, s)
+        if self.replan:
+            plan = self.make_plan()  # host: partition + LPT distribute + coalesce (or schedule)
+            plan.upload(self.d_plan, s)
+            self.plan = plan
+        plan = self.plan
+        if self.n_stages > 1:  # block-level pipeline: one launch per execution stage
+            for stg in range(self.n_stages):
+                f.block_attn_fwd_stage(plan, self.d_plan, stg, self.q, self.k, self.v, self.part_o, self.part_lse, s)
+        else:
+            f.block_attn_fwd(plan, self.d_plan, self.q, self.k, self.v, self.part_o, self.part_lse, s)
         rec(1)
         f.block_attn_merge(plan, self.d_plan, self.part_o, self.part_lse, self.o, self.lse, s)
         rec(2)
@@ -392,6 +405,7 @@ def bench_fcp(args):
         result["sweep"] = sweep(torch, fcp, W, args, dev, stream, flush, sustained)
     if rank == 0:
         result["solver"] = solver_report(fcp, W)
+        result["pipeline"] = pipeline_bench(torch, fcp, W, dev, stream, flush, sustained)
         result["balance"] = balance_report(W)
     if cpu is not None:
         result["cpu_baseline"] = cpu
@@ -498,6 +512,35 @@ def planner_compare(torch, fcp, W, dev, stream, flush, sustained):
                         "ms": round(ms, 3), "fwd_bwd_tflops": round(tf, 1), "frac_of_peak": round(tf / sustained, 4)})
             del st
             torch.cuda.empty_cache()
+    return out
+
+
+def pipeline_bench(torch, fcp, W, dev, stream, flush, sustained):
+    """The block-level pipeline with the bottom-up coalescer (Section 4.2, Figure 7, Table 2):
+    the forward launched one execution stage at a time (local work first, then `degree`
+    congestion-free sub-stages per stage), against coalesce degree c. Plans are built once,
+    outside the timed region, so the numbers isolate the kernels' side of the trade-off.
+    Workloads: the 32K causal sequence at 512-token blocks (64 blocks on 32 workers) and the
+    causal mixed batch (4K blocks, 16 workers)."""
+    out = []
+    for w in (W.block_sweep(512), W.causal_mixed()):
+        rows = []
+        for degree in (1, 4, 16, 64):
+            st = Step(fcp, torch, w, 1, dev, stream, pipeline=degree, replan=False)
+            times = timed_steps(torch, st, 3, 2, flush)
+            fwd = statistics.mean(t["fwd"] for t in times)
+            fm = statistics.mean(t["fwd"] + t["merge"] for t in times)
+            tot = statistics.mean(t["total"] for t in times)
+            v = st.plan.view()
+            rows.append({"degree": degree, "stages": st.n_stages, "runs": v["n_runs"],
+                         "fwd_ms": round(fwd, 3), "fwd_tflops": round(st.fwd_flops / (fwd * 1e-3) / 1e12, 1),
+                         "fwd_merge_tflops": round(st.fwd_flops / (fm * 1e-3) / 1e12, 1),
+                         "fwd_bwd_tflops": round((st.fwd_flops + st.bwd_flops) / (tot * 1e-3) / 1e12, 1),
+                         "fwd_bwd_frac_of_peak": round((st.fwd_flops + st.bwd_flops) / (tot * 1e-3) / 1e12
+                                                       / sustained, 4)})
+            del st
+            torch.cuda.empty_cache()
+        out.append({"workload": w.name, "workers": w.n_workers, "block": w.block_size, "by_degree": rows})
     return out
 
 

@@ -26,6 +26,7 @@ __all__ = [
     "lib",
     "library_path",
     "block_attn_fwd",
+    "block_attn_fwd_stage",
     "block_attn_merge",
     "block_attn_bwd",
     "block_attn_bwd_prologue",
@@ -75,7 +76,7 @@ class _Item(ctypes.Structure):
 
 class _Run(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("worker", "q_block", "q_tok0", "q_len", "item_begin", "item_end",
-                                              "part_row0", "reserved")]
+                                              "part_row0", "stage")]
 
 
 class _Transfer(ctypes.Structure):
@@ -84,7 +85,8 @@ class _Transfer(ctypes.Structure):
 
 class _View(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_seqs", "n_blocks", "n_segs", "n_items", "n_runs", "n_workers",
-                                              "block_size", "causal", "coalesce", "distributed")] + [
+                                              "block_size", "causal", "coalesce", "distributed",
+                                              "n_exec_stages")] + [
         (n, ctypes.c_int64) for n in ("total_tokens", "token_cap", "total_pairs", "partial_rows")] + [
         ("seqlens", ctypes.POINTER(ctypes.c_int32)),
         ("blocks", ctypes.POINTER(_Block)),
@@ -108,14 +110,17 @@ _SIGNATURES = {
     "fcp_distribute": (_ST, [_P, _I32, _I64]),
     "fcp_partition_ring": (_ST, [ctypes.POINTER(_I32), _I32, _I32, _I32, ctypes.POINTER(_P)]),
     "fcp_coalesce": (_ST, [_P, _I32]),
+    "fcp_schedule": (_ST, [_P, _I32, ctypes.POINTER(_I32)]),
     "fcp_plan_query": (_ST, [_P, ctypes.POINTER(_View)]),
     "fcp_solve_stages": (_ST, [_P]),
+    "fcp_set_stages": (_ST, [_P, ctypes.POINTER(_I32), _I32]),
     "fcp_plan_transfers": (_ST, [_P, ctypes.POINTER(ctypes.POINTER(_Transfer)), ctypes.POINTER(_I32),
                                  ctypes.POINTER(_I32)]),
     "fcp_plan_device_bytes": (_SZ, [_P]),
     "fcp_plan_upload": (_ST, [_P, _P, _SZ, _P]),
     "fcp_partial_sizes": (_ST, [_P, _I32, _I32, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "fcp_block_attn_fwd": (_ST, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
+    "fcp_block_attn_fwd_stage": (_ST, [_P, _P, _I32, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
     "fcp_block_attn_merge": (_ST, [_P, _P, _P, _P, _I32, _I32, _P, _P, _P]),
     "fcp_block_attn_bwd_prologue": (_ST, [_P, _P, _P, _I32, _I32, _P, _P, _P]),
     "fcp_bwd_workspace_bytes": (_SZ, [_P, _I32, _I32]),
@@ -175,7 +180,7 @@ class Plan:
     BLOCK_COLS = ("first_seg", "n_segs", "tokens", "seq", "seq_block_idx", "seq_nblocks", "zz_partner", "cost")
     SEG_COLS = ("seq", "start_in_seq", "len", "tok0")
     ITEM_COLS = ("worker", "q_block", "kv_block", "q_tok0", "q_len", "kv_tok0", "kv_len", "mask")
-    RUN_COLS = ("worker", "q_block", "q_tok0", "q_len", "item_begin", "item_end", "part_row0")
+    RUN_COLS = ("worker", "q_block", "q_tok0", "q_len", "item_begin", "item_end", "part_row0", "stage")
 
     def __init__(self, seqlens: Sequence[int], block_size: int, causal: bool):
         L = lib()
@@ -222,14 +227,31 @@ class Plan:
         _check(lib().fcp_coalesce(self._h, int(degree)), "fcp_coalesce")
         return self
 
+    def schedule(self, degree: int) -> int:
+        """Block-level pipeline with the bottom-up coalescer (fcp_schedule): items ordered by
+        the execution stage of their KV block, `degree` congestion-free sub-stages per stage.
+        Returns the number of execution stages."""
+        n = _I32()
+        _check(lib().fcp_schedule(self._h, int(degree), ctypes.byref(n)), "fcp_schedule")
+        return int(n.value)
+
     def solve(self) -> dict:
         """Congestion-free sub-stages (fcp_solve_stages): transfers as rows (kv_block, src, dst,
         stage, tokens) and the number of stages."""
-        L = lib()
-        _check(L.fcp_solve_stages(self._h), "fcp_solve_stages")
+        _check(lib().fcp_solve_stages(self._h), "fcp_solve_stages")
+        return self.transfers()
+
+    def set_stages(self, stages: Sequence[int]) -> None:
+        """Install a caller-supplied congestion-free plan: one sub-stage per data-flow edge,
+        edges in the order solve() lists them (fcp_set_stages)."""
+        arr = (_I32 * max(1, len(stages)))(*[int(x) for x in stages])
+        _check(lib().fcp_set_stages(self._h, arr, len(stages)), "fcp_set_stages")
+
+    def transfers(self) -> dict:
+        """The current congestion-free plan (fcp_plan_transfers), as solve() returns it."""
         ptr = ctypes.POINTER(_Transfer)()
         n, st = _I32(), _I32()
-        _check(L.fcp_plan_transfers(self._h, ctypes.byref(ptr), ctypes.byref(n), ctypes.byref(st)),
+        _check(lib().fcp_plan_transfers(self._h, ctypes.byref(ptr), ctypes.byref(n), ctypes.byref(st)),
                "fcp_plan_transfers")
         rows = _arr(ptr, n.value, None, ("kv_block", "src", "dst", "stage", "tokens"))
         return {"transfers": rows, "n_stages": int(st.value)}
@@ -238,7 +260,8 @@ class Plan:
         v = _View()
         _check(lib().fcp_plan_query(self._h, ctypes.byref(v)), "fcp_plan_query")
         out = {k: getattr(v, k) for k in ("n_seqs", "n_blocks", "n_segs", "n_items", "n_runs", "n_workers",
-                                           "block_size", "causal", "coalesce", "distributed", "total_tokens",
+                                           "block_size", "causal", "coalesce", "distributed", "n_exec_stages",
+                                           "total_tokens",
                                            "token_cap", "total_pairs", "partial_rows")}
         out["blocks"] = _arr(v.blocks, v.n_blocks, None, self.BLOCK_COLS)
         out["worker_of_block"] = _arr(v.blocks, v.n_blocks, None, ("worker",))[:, 0] if v.n_blocks else \
@@ -310,6 +333,22 @@ def block_attn_fwd(plan: Plan, d_plan, q, k, v, part_o, part_lse, stream=None) -
     _need(part_lse, torch.float32, None, "part_lse")
     _check(lib().fcp_block_attn_fwd(plan.handle, _ptr(d_plan), _ptr(q), _ptr(k), _ptr(v), hq, hkv, D, _ptr(part_o),
                                     _ptr(part_lse), _stream(stream)), "fcp_block_attn_fwd")
+
+
+def block_attn_fwd_stage(plan: Plan, d_plan, stage: int, q, k, v, part_o, part_lse, stream=None) -> None:
+    """Partial (O, LSE) of the runs of one execution stage (fcp_block_attn_fwd_stage)."""
+    import torch
+
+    hq, T, D = q.shape
+    hkv = k.shape[0]
+    _need(q, torch.bfloat16, None, "q")
+    _need(k, torch.bfloat16, (hkv, T, D), "k")
+    _need(v, torch.bfloat16, (hkv, T, D), "v")
+    _need(part_o, torch.float32, None, "part_o")
+    _need(part_lse, torch.float32, None, "part_lse")
+    _check(lib().fcp_block_attn_fwd_stage(plan.handle, _ptr(d_plan), int(stage), _ptr(q), _ptr(k), _ptr(v), hq, hkv,
+                                          D, _ptr(part_o), _ptr(part_lse), _stream(stream)),
+           "fcp_block_attn_fwd_stage")
 
 
 def block_attn_merge(plan: Plan, d_plan, part_o, part_lse, o, lse, stream=None) -> None:
@@ -401,15 +440,17 @@ def device_error(d_plan, stream=None) -> int:
 
 class FcpAttention:
     """A planned batch: the plan, its device image and the partial/workspace buffers, with
-    forward (fwd + merge) and backward over the same work list."""
+    forward (fwd + merge) and backward over the same work list. With ``pipeline=c`` the
+    plan is scheduled as the block-level pipeline with coalesce degree c (Plan.schedule) and
+    the forward launches one execution stage at a time before the merge."""
 
     def __init__(self, seqlens: Sequence[int], block_size: int, causal: bool, n_workers: int, hq: int, hkv: int,
                  head_dim: int, token_cap: Optional[int] = None, coalesce: int = 1, device="cuda",
-                 backward: bool = True):
-        import torch
-
+                 backward: bool = True, pipeline: Optional[int] = None):
         plan = Plan(seqlens, block_size, causal).distribute(n_workers, token_cap)
-        if coalesce != 1:
+        if pipeline is not None:
+            plan.schedule(pipeline)
+        elif coalesce != 1:
             plan.coalesce(coalesce)
         self._setup(plan, hq, hkv, head_dim, device, backward)
 
@@ -425,6 +466,7 @@ class FcpAttention:
         import torch
 
         self.plan = plan
+        self.n_stages = int(plan.view()["n_exec_stages"])
         self.hq, self.hkv, self.head_dim = hq, hkv, head_dim
         self.T = sum(int(x) for x in plan.seqlens)
         self.device = torch.device(device)
@@ -448,7 +490,11 @@ class FcpAttention:
             o = torch.empty((self.hq, self.T, self.head_dim), dtype=torch.bfloat16, device=self.device)
         if lse is None:
             lse = torch.empty((self.hq, self.T), dtype=torch.float32, device=self.device)
-        block_attn_fwd(self.plan, self.d_plan, q, k, v, self.part_o, self.part_lse, stream)
+        if self.n_stages > 1:
+            for st in range(self.n_stages):
+                block_attn_fwd_stage(self.plan, self.d_plan, st, q, k, v, self.part_o, self.part_lse, stream)
+        else:
+            block_attn_fwd(self.plan, self.d_plan, q, k, v, self.part_o, self.part_lse, stream)
         block_attn_merge(self.plan, self.d_plan, self.part_o, self.part_lse, o, lse, stream)
         return o, lse
 

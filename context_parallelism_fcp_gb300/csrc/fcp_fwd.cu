@@ -393,11 +393,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 template <int D>
-fcp_status launch_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
-                      int hq, int hkv, float* part_o, float* part_lse, cudaStream_t stream) {
+fcp_status launch_fwd(const fcp_plan* plan, const void* d_plan, int32_t unit_begin, int32_t n_units,
+                      const void* q, const void* k, const void* v, int hq, int hkv, float* part_o, float* part_lse,
+                      cudaStream_t stream) {
   using C = FwdCfg<D>;
   const DevLayout& L = plan->layout;
-  if (L.n_fwd_units == 0) return FCP_OK;
+  if (n_units == 0) return FCP_OK;
   const int64_t T = plan->total_tokens;
   CUtensorMap mq, mk, mv;
   fcp_status st;
@@ -407,7 +408,7 @@ fcp_status launch_fwd(const fcp_plan* plan, const void* d_plan, const void* q, c
   FwdArgs a;
   a.items = dev_array<fcp_item>(d_plan, L.items);
   a.runs = dev_array<fcp_run>(d_plan, L.runs);
-  a.units = dev_array<FwdUnit>(d_plan, L.fwd_units);
+  a.units = dev_array<FwdUnit>(d_plan, L.fwd_units) + unit_begin;
   a.part_o = part_o;
   a.part_lse = part_lse;
   a.part_rows = plan->partial_rows;
@@ -419,7 +420,7 @@ fcp_status launch_fwd(const fcp_plan* plan, const void* d_plan, const void* q, c
   a.err = dev_error_word(d_plan);
   FCP_CUDA_TRY(cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                "fwd smem attribute");
-  const long long grid = static_cast<long long>(L.n_fwd_units) * hkv * a.pairs_per_group;
+  const long long grid = static_cast<long long>(n_units) * hkv * a.pairs_per_group;
   if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
   fwd_kernel<D><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
   FCP_CUDA_TRY(cudaGetLastError(), "fwd launch");
@@ -431,17 +432,38 @@ fcp_status launch_fwd(const fcp_plan* plan, const void* d_plan, const void* q, c
 
 using namespace fcp;
 
-extern "C" fcp_status fcp_block_attn_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
-                                         const void* v, int32_t hq, int32_t hkv, int32_t head_dim, float* part_o,
-                                         float* part_lse, void* stream) {
+namespace {
+// The units [unit_begin, unit_begin + n_units) of the plan's forward unit list.
+fcp_status fwd_units(const fcp_plan* plan, const void* d_plan, int32_t unit_begin, int32_t n_units, const void* q,
+                     const void* k, const void* v, int32_t hq, int32_t hkv, int32_t head_dim, float* part_o,
+                     float* part_lse, void* stream) {
   if (plan == nullptr || d_plan == nullptr) return FCP_ERR_INVALID;
   if (!plan->distributed) return FCP_ERR_STATE;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return FCP_ERR_INVALID;
   if (head_dim != 64 && head_dim != 128) return FCP_ERR_UNSUPPORTED;
-  if (plan->layout.n_fwd_units == 0) return FCP_OK;
+  if (n_units == 0) return FCP_OK;
   if (!q || !k || !v || !part_o || !part_lse) return FCP_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(part_o)) return FCP_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (head_dim == 128) return launch_fwd<128>(plan, d_plan, q, k, v, hq, hkv, part_o, part_lse, s);
-  return launch_fwd<64>(plan, d_plan, q, k, v, hq, hkv, part_o, part_lse, s);
+  if (head_dim == 128)
+    return launch_fwd<128>(plan, d_plan, unit_begin, n_units, q, k, v, hq, hkv, part_o, part_lse, s);
+  return launch_fwd<64>(plan, d_plan, unit_begin, n_units, q, k, v, hq, hkv, part_o, part_lse, s);
+}
+}  // namespace
+
+extern "C" fcp_status fcp_block_attn_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
+                                         const void* v, int32_t hq, int32_t hkv, int32_t head_dim, float* part_o,
+                                         float* part_lse, void* stream) {
+  if (plan == nullptr) return FCP_ERR_INVALID;
+  return fwd_units(plan, d_plan, 0, plan->layout.n_fwd_units, q, k, v, hq, hkv, head_dim, part_o, part_lse, stream);
+}
+
+extern "C" fcp_status fcp_block_attn_fwd_stage(const fcp_plan* plan, const void* d_plan, int32_t stage,
+                                               const void* q, const void* k, const void* v, int32_t hq, int32_t hkv,
+                                               int32_t head_dim, float* part_o, float* part_lse, void* stream) {
+  if (plan == nullptr) return FCP_ERR_INVALID;
+  const std::vector<int32_t>& b = plan->layout.stage_unit_begin;
+  if (stage < 0 || static_cast<size_t>(stage) + 1 >= b.size()) return FCP_ERR_INVALID;
+  return fwd_units(plan, d_plan, b[stage], b[stage + 1] - b[stage], q, k, v, hq, hkv, head_dim, part_o, part_lse,
+                   stream);
 }

@@ -17,12 +17,13 @@ constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 
 // A query range with its runs (consecutive in the run list): what the merge reduces.
+// A query range: its tokens, how many runs reduce it and the first of its partial rows.
 struct QSeg {
-  int32_t tok0, len, run_begin, run_end;
+  int32_t tok0, len, n_runs, part_row0;
 };
 // Where the partials of one query token are: its k-th partial (k < count) is partial row
-// base + k * stride. The runs of a query range are consecutive and each owns q_len
-// contiguous partial rows, so stride is the range's length.
+// base + k * stride. The runs of a query range own consecutive blocks of q_len partial
+// rows, so stride is the range's length.
 struct TokPart {
   int32_t base, stride, count, reserved;
 };
@@ -54,6 +55,8 @@ struct DevLayout {
          bwd_units = 0, total = 0;
   int32_t n_qsegs = 0, n_fwd_units = 0, n_kvsegs = 0, n_kv_items = 0, n_bwd_units = 0;
   int32_t max_runs_per_qseg = 0;
+  // forward units of execution stage s: [stage_unit_begin[s], stage_unit_begin[s + 1])
+  std::vector<int32_t> stage_unit_begin;
 };
 
 // Device error codes written into DevHeader::error (kernel id * 16 + wait id).
@@ -84,6 +87,13 @@ struct fcp_plan {
   std::vector<fcp_item> items;
   std::vector<fcp_run> runs;
   int64_t partial_rows = 0;
+
+  // The work list in fcp_distribute's order (items holds it too unless fcp_schedule
+  // reordered them).
+  std::vector<fcp_item> work_list;
+  // Execution stage per item (fcp_schedule); empty: every item in stage 0.
+  std::vector<int32_t> item_stage;
+  int32_t n_exec_stages = 1;
 
   // Congestion-free solver output (fcp_solve_stages).
   bool solved = false;

@@ -7,6 +7,7 @@
 // Figure 4), Section 4.2 (bottom-up coalescer).
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <numeric>
 #include <set>
 #include <utility>
@@ -44,16 +45,32 @@ int32_t q_tiles_seeing(const fcp_item& it, int32_t kv_tile) {
   return n;
 }
 
+// Run ids grouped by query range (q_tok0, q_len), ranges in order of first appearance.
+std::vector<std::vector<int32_t>> runs_by_range(const std::vector<fcp_run>& runs) {
+  std::map<std::pair<int32_t, int32_t>, size_t> index;
+  std::vector<std::vector<int32_t>> out;
+  for (int32_t r = 0; r < static_cast<int32_t>(runs.size()); ++r) {
+    auto ins = index.insert({{runs[r].q_tok0, runs[r].q_len}, out.size()});
+    if (ins.second) out.emplace_back();
+    out[ins.first->second].push_back(r);
+  }
+  return out;
+}
+
+// Runs: consecutive items of one worker over one query range (and one execution stage),
+// at most `degree` items each (no limit when degree <= 0). Partial rows are allocated per
+// query range, in order of first appearance, so the runs of a range own consecutive
+// blocks of q_len rows.
 void build_runs(fcp_plan* p, int32_t degree) {
   p->runs.clear();
-  int64_t row = 0;
-  size_t i = 0;
   const size_t n = p->items.size();
+  auto stage_of = [&](size_t i) { return p->item_stage.empty() ? 0 : p->item_stage[i]; };
+  size_t i = 0;
   while (i < n) {
     const fcp_item& a = p->items[i];
     size_t j = i + 1;
-    while (j < n && static_cast<int32_t>(j - i) < degree && p->items[j].worker == a.worker &&
-           p->items[j].q_tok0 == a.q_tok0 && p->items[j].q_len == a.q_len)
+    while (j < n && (degree <= 0 || static_cast<int32_t>(j - i) < degree) && p->items[j].worker == a.worker &&
+           p->items[j].q_tok0 == a.q_tok0 && p->items[j].q_len == a.q_len && stage_of(j) == stage_of(i))
       ++j;
     fcp_run r{};
     r.worker = a.worker;
@@ -62,13 +79,21 @@ void build_runs(fcp_plan* p, int32_t degree) {
     r.q_len = a.q_len;
     r.item_begin = static_cast<int32_t>(i);
     r.item_end = static_cast<int32_t>(j);
-    r.part_row0 = static_cast<int32_t>(row);
+    r.part_row0 = -1;
+    r.stage = stage_of(i);
     const int32_t run_id = static_cast<int32_t>(p->runs.size());
     for (size_t t = i; t < j; ++t) p->items[t].run = run_id;
     p->runs.push_back(r);
-    row += a.q_len;
     i = j;
   }
+  // partial rows per query range
+  const auto ranges = runs_by_range(p->runs);
+  int64_t row = 0;
+  for (const auto& rg : ranges)
+    for (int32_t r : rg) {
+      p->runs[r].part_row0 = static_cast<int32_t>(row);
+      row += p->runs[r].q_len;
+    }
   p->partial_rows = row;
   p->coalesce = degree;
 }
@@ -81,24 +106,19 @@ void put(std::vector<uint8_t>& img, size_t off, const std::vector<T>& v) {
 // Device image: header, items, runs, query ranges with their runs, token -> partial rows,
 // forward units (longest first), key ranges with their items, backward units (longest first).
 bool build_image(fcp_plan* p) {
+  const auto ranges = runs_by_range(p->runs);
   std::vector<QSeg> qsegs;
-  for (int32_t r = 0; r < static_cast<int32_t>(p->runs.size()); ++r) {
-    const fcp_run& run = p->runs[r];
-    if (!qsegs.empty() && qsegs.back().tok0 == run.q_tok0 && qsegs.back().len == run.q_len) {
-      qsegs.back().run_end = r + 1;
-    } else {
-      qsegs.push_back(QSeg{run.q_tok0, run.q_len, r, r + 1});
-    }
-  }
   int32_t max_runs = 0;
   std::vector<TokPart> tok2part(static_cast<size_t>(p->total_tokens), TokPart{0, 0, 0, 0});
-  for (const QSeg& q : qsegs) {
-    max_runs = std::max(max_runs, q.run_end - q.run_begin);
-    const int32_t base = p->runs[q.run_begin].part_row0;
-    for (int32_t r = q.run_begin; r < q.run_end; ++r)
-      if (p->runs[r].part_row0 != base + (r - q.run_begin) * q.len) return false;  // rows must be contiguous
-    for (int32_t t = 0; t < q.len; ++t)
-      tok2part[static_cast<size_t>(q.tok0) + t] = TokPart{base + t, q.len, q.run_end - q.run_begin, 0};
+  for (const auto& rg : ranges) {
+    const fcp_run& r0 = p->runs[rg.front()];
+    const int32_t n = static_cast<int32_t>(rg.size());
+    max_runs = std::max(max_runs, n);
+    for (int32_t k = 0; k < n; ++k)
+      if (p->runs[rg[k]].part_row0 != r0.part_row0 + k * r0.q_len) return false;  // contiguous rows
+    qsegs.push_back(QSeg{r0.q_tok0, r0.q_len, n, r0.part_row0});
+    for (int32_t t = 0; t < r0.q_len; ++t)
+      tok2part[static_cast<size_t>(r0.q_tok0) + t] = TokPart{r0.part_row0 + t, r0.q_len, n, 0};
   }
 
   // forward units with their key-tile counts; longest first, ties in run/tile order
@@ -112,12 +132,17 @@ bool build_image(fcp_plan* p) {
     }
   }
   std::stable_sort(fu.begin(), fu.end(),
-                   [](const std::pair<int64_t, FwdUnit>& a, const std::pair<int64_t, FwdUnit>& b) {
+                   [&](const std::pair<int64_t, FwdUnit>& a, const std::pair<int64_t, FwdUnit>& b) {
+                     const int32_t sa = p->runs[a.second.run].stage, sb = p->runs[b.second.run].stage;
+                     if (sa != sb) return sa < sb;
                      return a.first > b.first;
                    });
   std::vector<FwdUnit> fwd_units;
   fwd_units.reserve(fu.size());
   for (auto& x : fu) fwd_units.push_back(x.second);
+  std::vector<int32_t> stage_begin(static_cast<size_t>(p->n_exec_stages) + 1, 0);
+  for (const FwdUnit& u : fwd_units) ++stage_begin[static_cast<size_t>(p->runs[u.run].stage) + 1];
+  for (int32_t st = 0; st < p->n_exec_stages; ++st) stage_begin[st + 1] += stage_begin[st];
 
   // key ranges, each with the items that read it (ordered by query offset)
   std::vector<int32_t> order(p->items.size());
@@ -195,6 +220,7 @@ bool build_image(fcp_plan* p) {
   L.n_kv_items = static_cast<int32_t>(kv_items.size());
   L.n_bwd_units = static_cast<int32_t>(bwd_units.size());
   L.max_runs_per_qseg = max_runs;
+  L.stage_unit_begin = std::move(stage_begin);
 
   for (const TokPart& tp : tok2part)
     if (tp.count <= 0) return false;  // every token must belong to exactly one query range
@@ -261,10 +287,13 @@ fcp_status finish_distribution(fcp_plan* p, const std::vector<int32_t>& owner, i
   p->token_cap = cap;
   p->load = std::move(load);
   p->tokens = std::move(tokens);
+  p->work_list = p->items;
   p->distributed = true;
   p->solved = false;
   p->transfers.clear();
   p->n_stages = 0;
+  p->item_stage.clear();
+  p->n_exec_stages = 1;
   build_runs(p, 1);
   if (!build_image(p)) {
     p->distributed = false;
@@ -478,11 +507,65 @@ fcp_status fcp_partition_ring(const int32_t* seqlens, int32_t n_seqs, int32_t n_
 fcp_status fcp_coalesce(fcp_plan* p, int32_t degree) {
   if (p == nullptr || degree <= 0) return FCP_ERR_INVALID;
   if (!p->distributed) return FCP_ERR_STATE;
+  if (!p->item_stage.empty()) {  // back to the work-list order of fcp_distribute
+    p->items = p->work_list;
+    p->item_stage.clear();
+    p->n_exec_stages = 1;
+  }
   build_runs(p, degree);
   if (!build_image(p)) {
     p->distributed = false;
     return FCP_ERR_STATE;
   }
+  return FCP_OK;
+}
+
+fcp_status fcp_schedule(fcp_plan* p, int32_t degree, int32_t* n_stages) {
+  if (p == nullptr || degree <= 0) return FCP_ERR_INVALID;
+  if (!p->distributed) return FCP_ERR_STATE;
+  if (!p->solved) {
+    fcp_status st = fcp_solve_stages(p);
+    if (st != FCP_OK) return st;
+  }
+  // sub-stage of each remote (KV block, receiver) pair
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> arrive(static_cast<size_t>(p->n_workers));
+  for (const fcp_transfer& t : p->transfers) arrive[t.dst].push_back({t.kv_block, t.stage});
+  p->items = p->work_list;
+  const size_t n = p->items.size();
+  std::vector<int32_t> stage(n, 0);
+  int32_t n_exec = 1;
+  for (size_t i = 0; i < n; ++i) {
+    const fcp_item& it = p->items[i];
+    if (p->blocks[it.kv_block].worker == it.worker) continue;  // local: stage 0
+    int32_t sub = -1;
+    for (const auto& a : arrive[it.worker])
+      if (a.first == it.kv_block) sub = a.second;
+    if (sub < 0) return FCP_ERR_STATE;  // every remote pair has a transfer
+    stage[i] = 1 + sub / degree;
+    n_exec = std::max(n_exec, stage[i] + 1);
+  }
+  std::vector<size_t> order(n);
+  std::iota(order.begin(), order.end(), size_t(0));
+  std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+    if (p->items[a].worker != p->items[b].worker) return p->items[a].worker < p->items[b].worker;
+    return stage[a] < stage[b];
+  });
+  std::vector<fcp_item> items(n);
+  std::vector<int32_t> item_stage(n);
+  for (size_t k = 0; k < n; ++k) {
+    items[k] = p->items[order[k]];
+    item_stage[k] = stage[order[k]];
+  }
+  p->items = std::move(items);
+  p->item_stage = std::move(item_stage);
+  p->n_exec_stages = n_exec;
+  build_runs(p, 0);
+  if (!build_image(p)) {
+    p->distributed = false;
+    return FCP_ERR_STATE;
+  }
+  p->coalesce = degree;
+  if (n_stages != nullptr) *n_stages = n_exec;
   return FCP_OK;
 }
 
@@ -499,6 +582,7 @@ fcp_status fcp_plan_query(const fcp_plan* p, fcp_plan_view* v) {
   v->causal = p->causal;
   v->coalesce = p->coalesce;
   v->distributed = p->distributed ? 1 : 0;
+  v->n_exec_stages = p->n_exec_stages;
   v->total_tokens = p->total_tokens;
   v->token_cap = p->token_cap;
   v->total_pairs = p->total_pairs;

@@ -10,6 +10,7 @@
 // condition holds in a regular bipartite graph) are peeled off one by one with
 // Hopcroft-Karp; the real edges of the k-th matching form sub-stage k.
 #include <algorithm>
+#include <set>
 #include <queue>
 #include <vector>
 
@@ -78,6 +79,24 @@ struct HopcroftKarp {
   }
 };
 
+constexpr int32_t kMaxSubStages = 1 << 24;
+
+// Edges of the data-flow graph: distinct (KV block, receiver) pairs whose block lives on
+// another worker, in work-list order, sub-stage unset.
+void build_edges(fcp_plan* p) {
+  p->transfers.clear();
+  std::vector<std::vector<int32_t>> pulled(static_cast<size_t>(p->n_workers));
+  for (const fcp_item& it : p->work_list) {
+    const int32_t src = p->blocks[it.kv_block].worker;
+    const int32_t dst = it.worker;
+    if (src == dst) continue;
+    auto& seen = pulled[dst];
+    if (std::find(seen.begin(), seen.end(), it.kv_block) != seen.end()) continue;
+    seen.push_back(it.kv_block);
+    p->transfers.push_back(fcp_transfer{it.kv_block, src, dst, -1, p->blocks[it.kv_block].tokens, 0});
+  }
+}
+
 }  // namespace
 }  // namespace fcp
 
@@ -89,18 +108,7 @@ fcp_status fcp_solve_stages(fcp_plan* p) {
   if (p == nullptr) return FCP_ERR_INVALID;
   if (!p->distributed) return FCP_ERR_STATE;
   const int32_t N = p->n_workers;
-  // edges: distinct (KV block, receiver) pairs whose block lives on another worker
-  p->transfers.clear();
-  std::vector<std::vector<int32_t>> pulled(static_cast<size_t>(N));
-  for (const fcp_item& it : p->items) {
-    const int32_t src = p->blocks[it.kv_block].worker;
-    const int32_t dst = it.worker;
-    if (src == dst) continue;
-    auto& seen = pulled[dst];
-    if (std::find(seen.begin(), seen.end(), it.kv_block) != seen.end()) continue;
-    seen.push_back(it.kv_block);
-    p->transfers.push_back(fcp_transfer{it.kv_block, src, dst, -1, p->blocks[it.kv_block].tokens, 0});
-  }
+  build_edges(p);
   std::vector<int32_t> deg_s(static_cast<size_t>(N), 0), deg_r(static_cast<size_t>(N), 0);
   for (const fcp_transfer& t : p->transfers) {
     ++deg_s[t.src];
@@ -162,6 +170,41 @@ fcp_status fcp_solve_stages(fcp_plan* p) {
     }
   }
   p->n_stages = delta;
+  p->solved = true;
+  return FCP_OK;
+}
+
+fcp_status fcp_set_stages(fcp_plan* p, const int32_t* stages, int32_t n_transfers) {
+  if (p == nullptr || n_transfers < 0 || (n_transfers > 0 && stages == nullptr)) return FCP_ERR_INVALID;
+  if (!p->distributed) return FCP_ERR_STATE;
+  build_edges(p);
+  p->solved = false;
+  if (static_cast<size_t>(n_transfers) != p->transfers.size()) {
+    p->transfers.clear();
+    set_last_error("fcp_set_stages: the stage count does not match the plan's transfers");
+    return FCP_ERR_INVALID;
+  }
+  int32_t n_stages = 0;
+  for (int32_t i = 0; i < n_transfers; ++i) {
+    if (stages[i] < 0 || stages[i] >= kMaxSubStages) {
+      p->transfers.clear();
+      set_last_error("fcp_set_stages: sub-stage out of range");
+      return FCP_ERR_INVALID;
+    }
+    n_stages = std::max(n_stages, stages[i] + 1);
+  }
+  // every sub-stage a matching: one send and one receive per worker
+  std::set<std::pair<int32_t, int32_t>> sends, recvs;
+  for (int32_t i = 0; i < n_transfers; ++i) {
+    const fcp_transfer& t = p->transfers[i];
+    if (!sends.insert({stages[i], t.src}).second || !recvs.insert({stages[i], t.dst}).second) {
+      p->transfers.clear();
+      set_last_error("fcp_set_stages: a sub-stage is not a matching");
+      return FCP_ERR_INVALID;
+    }
+  }
+  for (int32_t i = 0; i < n_transfers; ++i) p->transfers[i].stage = stages[i];
+  p->n_stages = n_stages;
   p->solved = true;
   return FCP_OK;
 }

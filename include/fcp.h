@@ -76,9 +76,11 @@ typedef struct {
 } fcp_item;
 
 /* A run: items [item_begin, item_end) of one worker over one query range, reduced into
- * one partial (O, LSE) at rows [part_row0, part_row0 + q_len) of the partial buffers. */
+ * one partial (O, LSE) at rows [part_row0, part_row0 + q_len) of the partial buffers.
+ * stage: the execution stage the run belongs to (0 unless fcp_schedule ordered the plan).
+ * The runs of one query range own consecutive partial rows, q_len apart. */
 typedef struct {
-  int32_t worker, q_block, q_tok0, q_len, item_begin, item_end, part_row0, reserved;
+  int32_t worker, q_block, q_tok0, q_len, item_begin, item_end, part_row0, stage;
 } fcp_run;
 
 /* One block transfer of the communication plan: KV block kv_block moves from its owner
@@ -91,10 +93,11 @@ typedef struct {
 typedef struct fcp_plan fcp_plan;
 
 /* Read-only view of a host plan. Pointers stay valid until the next mutating call on
- * the plan (fcp_distribute, fcp_coalesce) or fcp_plan_free. */
+ * the plan (fcp_distribute, fcp_coalesce, fcp_schedule) or fcp_plan_free.
+ * n_exec_stages: execution stages of the forward (1 unless fcp_schedule ran). */
 typedef struct {
   int32_t n_seqs, n_blocks, n_segs, n_items, n_runs, n_workers, block_size, causal, coalesce;
-  int32_t distributed;
+  int32_t distributed, n_exec_stages;
   int64_t total_tokens, token_cap, total_pairs, partial_rows;
   const int32_t* seqlens;
   const fcp_block* blocks;
@@ -154,10 +157,35 @@ fcp_status fcp_coalesce(fcp_plan* plan, int32_t degree);
  * distributed). Recomputed by each call; cleared by fcp_distribute. */
 fcp_status fcp_solve_stages(fcp_plan* plan);
 
+/* A caller-supplied congestion-free plan in place of the solver's (the pages note that the
+ * plan may be pre-computed elsewhere, Section 4.2): stages[i] is the sub-stage of the i-th
+ * edge of the plan's data-flow graph, the edges taken in the order fcp_solve_stages lists
+ * them (distinct (KV block, receiver) pairs, work-list order). n_transfers must equal the
+ * number of edges; every sub-stage must be a matching (each worker sends at most one block
+ * and receives at most one), each in [0, 2^24). The number of sub-stages becomes
+ * max(stages) + 1, which may exceed Delta. Errors: FCP_ERR_INVALID (count mismatch, a stage
+ * out of range, a sub-stage that is not a matching; the plan is left unsolved), FCP_ERR_STATE (not distributed). */
+fcp_status fcp_set_stages(fcp_plan* plan, const int32_t* stages, int32_t n_transfers);
+
 /* Read-only access to the solver's result: *transfers (n_transfers entries, valid until
  * the next mutating call) and the number of sub-stages. FCP_ERR_STATE if not solved. */
 fcp_status fcp_plan_transfers(const fcp_plan* plan, const fcp_transfer** transfers, int32_t* n_transfers,
                               int32_t* n_stages);
+
+/* Block-level pipeline with the bottom-up coalescer (Section 4.2, "Block-level pipelining",
+ * "Bottom-up coalescer", Figure 7): runs the solver if needed, then gives every work item
+ * the execution stage in which its KV block is available -- stage 0 for blocks the worker
+ * owns (local computation first, Section 4.3), 1 + s / degree for a block pulled in
+ * congestion-free sub-stage s, i.e. `degree` consecutive sub-stages merged into one stage
+ * -- reorders each worker's items by stage (stable, keeping the work-list order within a
+ * stage) and rebuilds the runs so that none crosses a stage; in each stage a worker
+ * receives at most `degree` blocks. *n_stages receives the number of execution stages.
+ * fcp_block_attn_fwd_stage then runs one stage at a time; fcp_block_attn_fwd runs them all.
+ * Errors: FCP_ERR_INVALID (degree <= 0), FCP_ERR_STATE (not distributed). */
+fcp_status fcp_schedule(fcp_plan* plan, int32_t degree, int32_t* n_stages);
+/* (fcp_schedule starts from the work list of fcp_distribute and uses the sub-stages in
+ * place when it is called; after fcp_solve_stages or fcp_set_stages, call it again.
+ * fcp_coalesce returns the plan to the unscheduled work-list order.) */
 
 /* Fill *view with read-only pointers into the plan. */
 fcp_status fcp_plan_query(const fcp_plan* plan, fcp_plan_view* view);
@@ -187,6 +215,14 @@ fcp_status fcp_partial_sizes(const fcp_plan* plan, int32_t hq, int32_t head_dim,
 fcp_status fcp_block_attn_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
                               const void* v, int32_t hq, int32_t hkv, int32_t head_dim, float* part_o,
                               float* part_lse, void* stream);
+
+/* The forward of one execution stage only (the runs whose stage field is `stage`), with
+ * the arguments of fcp_block_attn_fwd. Running every stage and then the merge gives the
+ * same result as fcp_block_attn_fwd + merge. Errors as fcp_block_attn_fwd, and
+ * FCP_ERR_INVALID for a stage outside [0, n_stages). */
+fcp_status fcp_block_attn_fwd_stage(const fcp_plan* plan, const void* d_plan, int32_t stage, const void* q,
+                                    const void* k, const void* v, int32_t hq, int32_t hkv, int32_t head_dim,
+                                    float* part_o, float* part_lse, void* stream);
 
 /* Associative log-sum-exp merge (Section 2.3) of every run's partial into the final
  * output: per (h, token) with partials s over its query range, m = max lse_s,

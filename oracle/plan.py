@@ -16,6 +16,8 @@ Pre-Training via FCP" (arXiv 2605.08524):
   tokens a worker holds.
 * Section 4.2 (bottom-up coalescer): consecutive block-level sub-stages of a
   worker can be merged into one execution stage of up to c blocks.
+* Section 4.2 (block-level pipelining, congestion-free solver, Figures 7 and 8) and
+  Section 4.3 (local computation first): the execution stage of each work item.
 
 Readings where the pages are silent (Appendix A.1 is not on the pages):
 
@@ -165,8 +167,8 @@ def coalesce(items: Sequence[tuple], degree: int) -> List[tuple]:
     """Runs of at most `degree` consecutive items of one worker sharing a query range.
 
     Returns runs as tuples (worker, q_block, q_tok0, q_len, item_begin, item_end,
-    part_row0), part_row0 being the run's first row in the partial-result buffer
-    (runs laid end to end, q_len rows each).
+    part_row0, stage), part_row0 being the run's first row in the partial-result buffer
+    (runs laid end to end, q_len rows each) and stage 0 (no pipeline schedule).
     """
     if degree <= 0:
         raise ValueError("coalesce degree must be positive")
@@ -179,7 +181,7 @@ def coalesce(items: Sequence[tuple], degree: int) -> List[tuple]:
         while (j < len(items) and j - i < degree and items[j][0] == w
                and items[j][3] == qtok and items[j][4] == qlen):
             j += 1
-        runs.append((w, qb, qtok, qlen, i, j, row))
+        runs.append((w, qb, qtok, qlen, i, j, row, 0))
         row += qlen
         i = j
     return runs
@@ -236,6 +238,99 @@ def stages_are_matchings(edges: Sequence[tuple], stage: Sequence[int], n_stages:
         sent.add((s, e[1]))
         got.add((s, e[2]))
     return True
+
+
+def solve_stages(edges: Sequence[tuple], n_workers: int) -> List[int]:
+    """A split of the data-flow edges into Delta matchings (Section 4.2, congestion-free
+    solver: the optimum number of sub-stages is Delta, Lemmas 1 and 2), by Koenig's
+    edge-colouring argument for bipartite multigraphs: colour the edges one at a time; for
+    edge (u, v) take a colour a free at sender u and a colour b free at receiver v (both
+    exist, each has fewer than Delta coloured edges); if a is not free at v, swap a and b
+    along the path from v that alternates b, a, b, ... edges (it cannot reach u), after
+    which a is free at both ends. Colour c is sub-stage c. Returns the stage of every edge."""
+    delta = max_degree(edges, n_workers)
+    # colour -> edge at each endpoint; senders are ("s", w), receivers ("r", w)
+    at: Dict[tuple, Dict[int, int]] = {}
+    stage = [-1] * len(edges)
+
+    def ends(i):
+        return ("s", edges[i][1]), ("r", edges[i][2])
+
+    for i in range(len(edges)):
+        u, v = ends(i)
+        at.setdefault(u, {})
+        at.setdefault(v, {})
+        a = min(c for c in range(delta) if c not in at[u])
+        b = min(c for c in range(delta) if c not in at[v])
+        if a in at[v]:
+            # the a/b alternating path from v, starting with its a-edge
+            path = []
+            node, colour = v, a
+            while colour in at[node]:
+                e = at[node][colour]
+                path.append(e)
+                x, y = ends(e)
+                node = y if node == x else x
+                colour = b if colour == a else a
+            for e in path:
+                x, y = ends(e)
+                del at[x][stage[e]]
+                del at[y][stage[e]]
+            for e in path:
+                x, y = ends(e)
+                stage[e] = b if stage[e] == a else a
+                at[x][stage[e]] = e
+                at[y][stage[e]] = e
+        stage[i] = a
+        at[u][a] = i
+        at[v][a] = i
+    return stage
+
+
+def schedule(part: Dict[str, list], dist: Dict[str, list], edges: Sequence[tuple], stage: Sequence[int],
+             degree: int) -> Dict[str, list]:
+    """The block-level pipeline with the bottom-up coalescer (Section 4.2, Figure 7; local
+    computation first, Section 4.3). A work item runs in execution stage 0 when its worker
+    owns the KV block, else in stage 1 + s // degree, s being the sub-stage in which the
+    block reaches the worker (`degree` consecutive sub-stages merged into one stage). Each
+    worker's items are taken stage by stage, keeping work-list order inside a stage. A run
+    is a maximal group of consecutive items of one worker, query range and stage; the runs
+    of one query range take consecutive q_len-row slices of the partial buffer, ranges in
+    order of first appearance.
+
+    Returns {"items", "item_stage", "runs" (as `coalesce`'s tuples, stage filled),
+    "n_stages", "partial_rows"}."""
+    if degree <= 0:
+        raise ValueError("coalesce degree must be positive")
+    owner = dist["worker_of_block"]
+    arrive = {(e[0], e[2]): s for e, s in zip(edges, stage)}
+    items = list(dist["items"])
+    st = []
+    for it in items:
+        w, kb = it[0], it[2]
+        st.append(0 if owner[kb] == w else 1 + arrive[(kb, w)] // degree)
+    order = sorted(range(len(items)), key=lambda i: (items[i][0], st[i], i))
+    items = [items[i] for i in order]
+    st = [st[i] for i in order]
+    runs = []
+    i = 0
+    while i < len(items):
+        w, qb, _, qtok, qlen = items[i][:5]
+        j = i + 1
+        while j < len(items) and items[j][0] == w and items[j][3] == qtok and items[j][4] == qlen and st[j] == st[i]:
+            j += 1
+        runs.append([w, qb, qtok, qlen, i, j, -1, st[i]])
+        i = j
+    ranges: Dict[tuple, List[int]] = {}
+    for r, run in enumerate(runs):
+        ranges.setdefault((run[2], run[3]), []).append(r)
+    row = 0
+    for rs in ranges.values():  # insertion order: first appearance
+        for r in rs:
+            runs[r][6] = row
+            row += runs[r][3]
+    return {"items": items, "item_stage": st, "runs": [tuple(r) for r in runs],
+            "n_stages": 1 + max(st, default=0), "partial_rows": row}
 
 
 def worker_order(part: Dict[str, list], dist: Dict[str, list], n_workers: int) -> List[int]:

@@ -21,13 +21,14 @@ O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
 G_MAX_REL, G_MEAN_REL, G_MEAN_ABS = 5e-2, 1e-2, 1e-5
 
 
-def run_path(fcp, w: W.Workload, coalesce=None, backward=None, device="cuda"):
+def run_path(fcp, w: W.Workload, coalesce=None, backward=None, device="cuda", pipeline=None):
     backward = w.backward if backward is None else backward
     dev = torch.device(device)
     q, k, v = W.make_qkv(w, device=dev)
     do = W.make_dout(w, device=dev) if backward else None
     att = fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, w.hq, w.hkv, w.head_dim,
-                           token_cap=w.token_cap, coalesce=coalesce or w.coalesce, device=dev, backward=backward)
+                           token_cap=w.token_cap, coalesce=coalesce or w.coalesce, device=dev, backward=backward,
+                           pipeline=pipeline)
     o, lse = att.forward(q, k, v)
     grads = att.backward(q, k, v, o, lse, do) if backward else None
     torch.cuda.synchronize()
