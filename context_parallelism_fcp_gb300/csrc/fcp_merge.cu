@@ -126,12 +126,14 @@ __global__ void __launch_bounds__(32 * kRowWarps)
   int nr[R], stride[R], start[R + 1];
   long long off[R];
   start[0] = 0;
+  bool single = true;  // no row has more than one partial (rows past T have none)
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     off[i] = hoff + __shfl_sync(0xffffffffu, info.x, i);
     stride[i] = __shfl_sync(0xffffffffu, info.y, i);
     nr[i] = __shfl_sync(0xffffffffu, info.z, i);
     start[i + 1] = start[i] + nr[i];
+    single = single && nr[i] <= 1;
   }
   const int P = start[R];
 
@@ -170,9 +172,10 @@ __global__ void __launch_bounds__(32 * kRowWarps)
       }
     }
     const float l = lane < P ? __ldg(part_lse + prow) : -INFINITY;
-    if (P == R) {
+    if (single) {
       // one partial per row (every row's range has a single run): the merge is the identity
-      // for rows with a finite LSE; rows without any visible key give O = 0, LSE = -inf
+      // for rows with a finite LSE; rows without any visible key give O = 0, LSE = -inf.
+      // Rows past T (no partial) come last, so pair i is row i for every stored row.
 #pragma unroll
       for (int i = 0; i < R; ++i) {
         const long long t = t0 + i;

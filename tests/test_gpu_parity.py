@@ -63,11 +63,14 @@ def _merge_expected(w, part_o, part_lse, coalesce):
 
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("neg_inf", [0.0, 0.3])
-@pytest.mark.parametrize("seqlens,coalesce", [([1000, 300, 2049, 17], 2), ([2304, 40, 3], 1)],
-                         ids=["few partials", "many partials"])
+@pytest.mark.parametrize("seqlens,coalesce", [([1000, 300, 2049, 17], 2), ([2304, 40, 3], 1), ([260], 1),
+                                              ([770], 1)],
+                         ids=["few partials", "many partials", "tail 4x2", "tail 2x4"])
 def test_merge_kernel_matches_oracle_merge(fcp, head_dim, neg_inf, seqlens, coalesce):
     """Partials of up to 9 runs per row: the second case puts 36 partials on the 4 rows one
-    warp merges, which takes the kernel's general path."""
+    warp merges, which takes the kernel's general path. The tail cases end the batch inside
+    a warp's 8 rows with exactly 8 partials on the valid rows (4 rows x 2, 2 rows x 4), which
+    must not be taken for one partial per row."""
     w = W.Workload("merge", seqlens, 256, 4, 2, head_dim, 3, True)
     att = fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, w.hq, w.hkv, w.head_dim,
                            coalesce=coalesce, backward=False)
