@@ -416,38 +416,91 @@ def bench_fcp(args):
 
 
 def e2e(torch, fcp, w, args, dev, stream, step):
-    """The same metric with host buffers: each step copies Q, K, V, dO from pinned host memory,
-    runs the path through the public API and copies O, LSE, dQ, dK, dV back."""
+    """The same metric with host buffers, through the public API (FcpAttention): each step
+    copies Q, K, V, dO from pinned host memory, runs forward and backward and copies O, LSE,
+    dQ, dK, dV back to pinned host memory. The copies run on their own streams, one per
+    direction, into and out of two alternating device buffer sets, so step i+1's inputs
+    arrive and step i's results leave while step i computes; dO travels during step i's
+    forward and O, LSE during its backward. Every step's copies are inside the timed region.
+    `serial` is the same loop with every copy on the compute stream."""
     hq, hkv, T, D = w.hq, w.hkv, w.total_tokens, w.head_dim
     hin = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.do)]
-    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (step.o, step.lse, step.dq, step.dk, step.dv)]
-    dq_in = [torch.empty_like(t) for t in (step.q, step.k, step.v, step.do)]
+    outs = (step.o, step.lse, step.dq, step.dk, step.dv)
+    hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(2)]
+    din = [[torch.empty_like(t) for t in (step.q, step.k, step.v, step.do)] for _ in range(2)]
+    dout = [[torch.empty_like(t) for t in outs] for _ in range(2)]
     att = fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, hq, hkv, D, token_cap=w.token_cap,
                            coalesce=args.coalesce, device=dev)
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    qkv_in, do_in, fwd_done, bwd_done, out_free = ([ev() for _ in range(2)] for _ in range(5))
 
-    def one():
-        with torch.cuda.stream(stream):
-            for d, h in zip(dq_in, hin):
+    def pipelined(i):
+        b = i & 1
+        q, k, v, do = din[b]
+        o, lse, dq, dk, dv = dout[b]
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(bwd_done[b])  # set b's inputs were last read by step i-2
+            for d, h in zip(din[b][:3], hin[:3]):
                 d.copy_(h, non_blocking=True)
-            o, lse = att.forward(*dq_in[:3], stream=stream)
-            dq, dk, dv = att.backward(dq_in[0], dq_in[1], dq_in[2], o, lse, dq_in[3], stream=stream)
-            for h, d in zip(hout, (o, lse, dq, dk, dv)):
+            qkv_in[b].record(h2d)
+            do.copy_(hin[3], non_blocking=True)
+            do_in[b].record(h2d)
+        stream.wait_event(qkv_in[b])
+        if i >= 2:
+            stream.wait_event(out_free[b])  # set b's outputs were last read by step i-2's copies
+        att.forward(q, k, v, o=o, lse=lse, stream=stream)
+        fwd_done[b].record(stream)
+        stream.wait_event(do_in[b])
+        att.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, stream=stream)
+        bwd_done[b].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(fwd_done[b])
+            for h, d in zip(hout[b][:2], (o, lse)):
+                h.copy_(d, non_blocking=True)
+            d2h.wait_event(bwd_done[b])
+            for h, d in zip(hout[b][2:], (dq, dk, dv)):
+                h.copy_(d, non_blocking=True)
+            out_free[b].record(d2h)
+
+    def serial(i):
+        q, k, v, do = din[0]
+        o, lse, dq, dk, dv = dout[0]
+        with torch.cuda.stream(stream):
+            for d, h in zip(din[0], hin):
+                d.copy_(h, non_blocking=True)
+            att.forward(q, k, v, o=o, lse=lse, stream=stream)
+            att.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, stream=stream)
+            for h, d in zip(hout[0], (o, lse, dq, dk, dv)):
                 h.copy_(d, non_blocking=True)
 
-    for _ in range(args.warmup):
-        one()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        one()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    def timed(one):
+        for i in range(args.warmup):
+            one(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d.wait_event(e0)
+        d2h.wait_event(e0)
+        for i in range(args.steps):
+            one(args.warmup + i)
+        for b in range(2):
+            stream.wait_event(out_free[b])
+        stream.wait_stream(d2h)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    ms = timed(pipelined)
+    ms_serial = timed(serial)
     flops = step.fwd_flops + step.bwd_flops
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
-            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)}
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout[0]),
+            "copies": "h2d and d2h streams, double-buffered: step i+1's inputs and step i's results "
+                      "move while step i computes",
+            "serial": {"value": round(flops / (ms_serial * 1e-3) / 1e12, 2), "ms_per_step": round(ms_serial, 3)}}
 
 
 def sweep(torch, fcp, W, args, dev, stream, flush, sustained):
