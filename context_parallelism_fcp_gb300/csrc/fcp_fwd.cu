@@ -6,8 +6,11 @@
 // partial (O normalised over those keys, natural LSE) -- the per-slice partial results of
 // Section 2.3 that the merge reduces.
 //
-// CTA = one 128-row query tile of one run, for two query heads of the same KV group (two
-// "tiles" t = 0, 1 that share every K/V tile loaded into shared memory). 10 warps:
+// Work tile = one 128-row query tile of one run, for two query heads of the same KV group
+// (two "heads" t = 0, 1 that share every K/V tile loaded into shared memory). The kernel is
+// persistent: one CTA per SM takes tiles (sorted longest first) from a global counter, and
+// the next tile's Q load, the K/V ring and the previous tile's partial stores overlap the
+// current tile's MMAs. 10 warps:
 //   warps 0-3  softmax of tile 0: thread = query row = TMEM lane
 //   warps 4-7  softmax of tile 1
 //   warp  8    TMA producer: Q tiles once, then K and V tiles through 2-stage rings
@@ -35,6 +38,8 @@ struct FwdArgs {
   const fcp_item* items;
   const fcp_run* runs;
   const FwdUnit* units;
+  long long n_tiles;                 // units x KV heads x head pairs
+  unsigned long long* next_tile;     // tile counter, zero at launch
   float* part_o;
   float* part_lse;
   long long part_rows;
@@ -45,16 +50,25 @@ struct FwdArgs {
 
 enum : int {
   B_QFULL = 0,
-  B_KFULL = 1,   // 2 stages
-  B_KEMPTY = 3,  // 2 stages
-  B_VFULL = 5,
-  B_VEMPTY = 7,
-  B_SFULL = 9,   // per tile
-  B_PFULL = 11,  // per tile
-  B_ODONE = 13,  // per tile
-  B_DRAIN = 15,
-  B_COUNT = 16
+  B_QEMPTY = 1,  // the S MMAs of a tile have read Q
+  B_KFULL = 2,   // 2 stages
+  B_KEMPTY = 4,  // 2 stages
+  B_VFULL = 6,
+  B_VEMPTY = 8,
+  B_SFULL = 10,  // per tile
+  B_PFULL = 12,  // per tile
+  B_ODONE = 14,  // per tile
+  B_OFREE = 16,  // per tile: the epilogue has read O_t out of TMEM
+  B_DRAIN = 18,
+  B_TFULL = 19,   // 2 slots: the producer has published the next tile index
+  B_TEMPTY = 21,  // 2 slots: the MMA warp and the 8 softmax warps have read it
+  B_COUNT = 23
 };
+
+// barrier area: mbarriers, abort flag, TMEM base, then the 2-slot tile ring (48 bytes a slot)
+constexpr int kTileSlotOff = 256;
+constexpr int kBarArea = kTileSlotOff + 2 * 48;
+static_assert(B_COUNT * 8 + 8 <= kTileSlotOff, "barrier area");
 
 template <int D>
 struct FwdCfg {
@@ -66,7 +80,7 @@ struct FwdCfg {
   static constexpr int kV = 4 * kTileBytes;
   static constexpr int kBar = 6 * kTileBytes;
   // at least half the SM's shared memory, so one CTA per SM holds all 512 TMEM columns
-  static constexpr int kSmemBytes = (kBar + 256) > 118 * 1024 ? (kBar + 256) : 118 * 1024;
+  static constexpr int kSmemBytes = (kBar + kBarArea) > 118 * 1024 ? (kBar + kBarArea) : 118 * 1024;
   static constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kTileM, D, false, true);
 };
@@ -96,21 +110,62 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
   const int per_unit = a.hkv * a.pairs_per_group;
-  const int unit_idx = blockIdx.x / per_unit;
-  const int rem = blockIdx.x - unit_idx * per_unit;
-  const int kvh = rem / a.pairs_per_group;
-  const int pair = rem - kvh * a.pairs_per_group;
-  const int h0 = kvh * a.group + 2 * pair;
-  const bool has_h1 = 2 * pair + 1 < a.group;
-  const int h1 = has_h1 ? h0 + 1 : h0;
-  const FwdUnit unit = a.units[unit_idx];
-  const fcp_run run = a.runs[unit.run];
-  const int qt = unit.q_tile;
+
+  // Tiles (unit, KV head, head pair), sorted longest first, are handed out dynamically: the
+  // producer takes the next index from a global counter, decodes it and publishes it in a
+  // 2-slot ring that the MMA warp and the softmax warps read (valid = 0: no tile left).
+  struct Tile {
+    int item_begin, item_end, q_tok0, q_len, part_row0, qt, kvh, h0, h1, has_h1, valid, pad;
+  };
+  Tile* tile_slot = reinterpret_cast<Tile*>(smem + C::kBar + kTileSlotOff);
+  auto decode = [&](long long w) -> Tile {
+    Tile t;
+    const int unit_idx = static_cast<int>(w / per_unit);
+    const int rem = static_cast<int>(w - static_cast<long long>(unit_idx) * per_unit);
+    t.kvh = rem / a.pairs_per_group;
+    const int pair = rem - t.kvh * a.pairs_per_group;
+    t.h0 = t.kvh * a.group + 2 * pair;
+    t.has_h1 = 2 * pair + 1 < a.group;
+    t.h1 = t.has_h1 ? t.h0 + 1 : t.h0;
+    const FwdUnit unit = a.units[unit_idx];
+    const fcp_run run = a.runs[unit.run];
+    t.item_begin = run.item_begin;
+    t.item_end = run.item_end;
+    t.q_tok0 = run.q_tok0;
+    t.q_len = run.q_len;
+    t.part_row0 = run.part_row0;
+    t.qt = unit.q_tile;
+    t.valid = 1;
+    t.pad = 0;
+    return t;
+  };
+  // consumer side: the tile of round u (valid = -1 when a wait gave up)
+  auto next_tile = [&](int u, int code) -> Tile {
+    Tile t;
+    t.valid = -1;
+    if (__all_sync(0xffffffffu, mbar_wait(bar(B_TFULL + (u & 1)), (u >> 1) & 1, abort_flag, a.err, code))) {
+      const volatile Tile* src = tile_slot + (u & 1);
+      t.item_begin = src->item_begin;
+      t.item_end = src->item_end;
+      t.q_tok0 = src->q_tok0;
+      t.q_len = src->q_len;
+      t.part_row0 = src->part_row0;
+      t.qt = src->qt;
+      t.kvh = src->kvh;
+      t.h0 = src->h0;
+      t.h1 = src->h1;
+      t.has_h1 = src->has_h1;
+      t.valid = src->valid;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_TEMPTY + (u & 1)));
+    }
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
@@ -119,8 +174,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_PFULL + s), kTileM);
       mbar_init(bar(B_ODONE + s), 1);
+      mbar_init(bar(B_OFREE + s), kTileM);
     }
     mbar_init(bar(B_DRAIN), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(B_TFULL + k), 1);
+      mbar_init(bar(B_TEMPTY + k), 9);
+    }
     *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
     mbar_fence_init();
   }
@@ -136,36 +196,65 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
+    // Q of tile u+1 is loaded as soon as the S MMAs of tile u have read Q; K and V stream
+    // through 2-stage rings whose slots are counted across tiles (J).
     if (lane == 0 && !skip) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const int qrow = run.q_tok0 + qt * kTileM;
-      mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::kTileBytes);
-#pragma unroll
-      for (int p = 0; p < C::kPanels; ++p) {
-        tma_load_3d(sb + C::kQ0 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, h0);
-        tma_load_3d(sb + C::kQ1 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, h1);
-      }
-      int j = 0;
+      int J = 0;
       bool ok = true;
-      for (int ii = run.item_begin; ii < run.item_end && ok; ++ii) {
-        const fcp_item itm = a.items[ii];
-        const int nkt = kv_tiles(itm, qt);
-        for (int kt = 0; kt < nkt; ++kt, ++j) {
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          const int kvrow = itm.kv_tok0 + kt * kTileN;
-          if (!mbar_wait(bar(B_KEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_KFULL + s), C::kTileBytes);
+      for (int u = 0; ok; ++u) {
+        const int k = u & 1;
+        if (!mbar_wait(bar(B_TEMPTY + k), ((u >> 1) & 1) ^ 1, abort_flag, a.err, kErrFwdWait + 13)) break;
+        unsigned long long got = atomicAdd(a.next_tile, 1ull);
+        Tile T;
+        T.valid = 0;
+        if (got < static_cast<unsigned long long>(a.n_tiles)) T = decode(static_cast<long long>(got));
+        {
+          volatile Tile* dst = tile_slot + k;
+          dst->item_begin = T.item_begin;
+          dst->item_end = T.item_end;
+          dst->q_tok0 = T.q_tok0;
+          dst->q_len = T.q_len;
+          dst->part_row0 = T.part_row0;
+          dst->qt = T.qt;
+          dst->kvh = T.kvh;
+          dst->h0 = T.h0;
+          dst->h1 = T.h1;
+          dst->has_h1 = T.has_h1;
+          dst->valid = T.valid;
+        }
+        mbar_arrive(bar(B_TFULL + k));
+        if (!T.valid) break;
+        if (!mbar_wait(bar(B_QEMPTY), (u & 1) ^ 1, abort_flag, a.err, kErrFwdWait + 11)) break;
+        const int qrow = T.q_tok0 + T.qt * kTileM;
+        mbar_arrive_expect_tx(bar(B_QFULL), 2 * C::kTileBytes);
 #pragma unroll
-          for (int p = 0; p < C::kPanels; ++p)
-            tma_load_3d(sb + C::kK + s * C::kTileBytes + p * kPanelBytes, &tmK, bar(B_KFULL + s), p * 64, kvrow, kvh);
-          if (!mbar_wait(bar(B_VEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 2)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_VFULL + s), C::kTileBytes);
+        for (int p = 0; p < C::kPanels; ++p) {
+          tma_load_3d(sb + C::kQ0 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, T.h0);
+          tma_load_3d(sb + C::kQ1 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, T.h1);
+        }
+        for (int ii = T.item_begin; ii < T.item_end && ok; ++ii) {
+          const fcp_item itm = a.items[ii];
+          const int nkt = kv_tiles(itm, T.qt);
+          for (int kt = 0; kt < nkt; ++kt, ++J) {
+            const int s = J & 1;
+            const uint32_t ph = (J >> 1) & 1;
+            const int kvrow = itm.kv_tok0 + kt * kTileN;
+            if (!mbar_wait(bar(B_KEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 1)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar(B_KFULL + s), C::kTileBytes);
 #pragma unroll
-          for (int p = 0; p < C::kPanels; ++p)
-            tma_load_3d(sb + C::kV + s * C::kTileBytes + p * kPanelBytes, &tmV, bar(B_VFULL + s), p * 64, kvrow, kvh);
+            for (int p = 0; p < C::kPanels; ++p)
+              tma_load_3d(sb + C::kK + s * C::kTileBytes + p * kPanelBytes, &tmK, bar(B_KFULL + s), p * 64, kvrow,
+                          T.kvh);
+            if (!mbar_wait(bar(B_VEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 2)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar(B_VFULL + s), C::kTileBytes);
+#pragma unroll
+            for (int p = 0; p < C::kPanels; ++p)
+              tma_load_3d(sb + C::kV + s * C::kTileBytes + p * kPanelBytes, &tmV, bar(B_VFULL + s), p * 64, kvrow,
+                          T.kvh);
+          }
         }
       }
     }
@@ -194,51 +283,62 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int kk = 0; kk < kTileN / 16; ++kk)
           mma_ts_w(d, p + kk * 8, sdesc_sw128(vbase + kk * 2048, kPanelBytes, 1024), C::kIdescPV, (acc || kk > 0));
       };
-      bool ok = wwait(bar(B_QFULL), 0, kErrFwdWait + 3);
-      tc_fence_after();
-      int j = 0;
-      for (int ii = run.item_begin; ii < run.item_end && ok; ++ii) {
-        const fcp_item itm = a.items[ii];
-        const int nkt = kv_tiles(itm, qt);
-        for (int kt = 0; kt < nkt && ok; ++kt, ++j) {
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!wwait(bar(B_KFULL + s), ph, kErrFwdWait + 4)) { ok = false; break; }
+      // PV of global key tile J-1 (local index jl-1) for both heads; the first PV of a tile
+      // overwrites O_t, which the previous tile's epilogue must have read out first
+      auto finish_pv = [&](int J, int jl, int u, bool last) -> bool {
+        const int ps = (J - 1) & 1;
+        if (!wwait(bar(B_VFULL + ps), ((J - 1) >> 1) & 1, kErrFwdWait + 5)) return false;
+        for (int t = 0; t < 2; ++t) {
+          if (!wwait(bar(B_PFULL + t), (J - 1) & 1, kErrFwdWait + 6)) return false;
+          if (jl == 1 && u > 0 && !wwait(bar(B_OFREE + t), (u - 1) & 1, kErrFwdWait + 12)) return false;
           tc_fence_after();
-          for (int t = 0; t < 2; ++t) {
-            if (j > 0) {
-              const int ps = (j - 1) & 1;
-              if (t == 0) {
-                if (!wwait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, kErrFwdWait + 5)) {
+          issue_pv(t, ps, jl - 1 > 0);
+          tc_commit_w(bar(B_ODONE + t));
+          if (t == 1 && last) tc_commit_w(bar(B_VEMPTY + ps));
+        }
+        return true;
+      };
+      bool ok = true;
+      int J = 0;
+      for (int u = 0; ok; ++u) {
+        const Tile T = next_tile(u, kErrFwdWait + 14);
+        if (T.valid <= 0) break;
+        ok = wwait(bar(B_QFULL), u & 1, kErrFwdWait + 3);
+        if (!ok) break;
+        tc_fence_after();
+        int jl = 0;
+        for (int ii = T.item_begin; ii < T.item_end && ok; ++ii) {
+          const fcp_item itm = a.items[ii];
+          const int nkt = kv_tiles(itm, T.qt);
+          for (int kt = 0; kt < nkt && ok; ++kt, ++J, ++jl) {
+            const int s = J & 1;
+            const uint32_t ph = (J >> 1) & 1;
+            if (!wwait(bar(B_KFULL + s), ph, kErrFwdWait + 4)) { ok = false; break; }
+            tc_fence_after();
+            for (int t = 0; t < 2; ++t) {
+              if (jl > 0) {
+                const int ps = (J - 1) & 1;
+                if (t == 0 && !wwait(bar(B_VFULL + ps), ((J - 1) >> 1) & 1, kErrFwdWait + 5)) { ok = false; break; }
+                if (!wwait(bar(B_PFULL + t), (J - 1) & 1, kErrFwdWait + 6)) { ok = false; break; }
+                if (jl == 1 && u > 0 && !wwait(bar(B_OFREE + t), (u - 1) & 1, kErrFwdWait + 12)) {
                   ok = false;
                   break;
                 }
+                tc_fence_after();
+                issue_pv(t, ps, jl - 1 > 0);
+                tc_commit_w(bar(B_ODONE + t));
+                if (t == 1) tc_commit_w(bar(B_VEMPTY + ps));
               }
-              if (!wwait(bar(B_PFULL + t), (j - 1) & 1, kErrFwdWait + 6)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              issue_pv(t, ps, j - 1 > 0);
-              tc_commit_w(bar(B_ODONE + t));
-              if (t == 1) tc_commit_w(bar(B_VEMPTY + ps));
+              issue_s(t, s);
+              tc_commit_w(bar(B_SFULL + t));
             }
-            issue_s(t, s);
-            tc_commit_w(bar(B_SFULL + t));
+            if (ok) tc_commit_w(bar(B_KEMPTY + s));
           }
-          if (ok) tc_commit_w(bar(B_KEMPTY + s));
         }
-      }
-      if (ok && j > 0) {
-        const int ps = (j - 1) & 1;
-        ok = wwait(bar(B_VFULL + ps), ((j - 1) >> 1) & 1, kErrFwdWait + 5);
-        for (int t = 0; t < 2 && ok; ++t) {
-          ok = wwait(bar(B_PFULL + t), (j - 1) & 1, kErrFwdWait + 6);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, ps, j - 1 > 0);
-          tc_commit_w(bar(B_ODONE + t));
-        }
+        if (!ok) break;
+        // every S of this tile has been issued: Q is free once they complete
+        tc_commit_w(bar(B_QEMPTY));
+        if (jl > 0) ok = finish_pv(J, jl, u, true);
       }
       // every issued MMA has completed once the drain barrier fires
       tc_commit_w(bar(B_DRAIN));
@@ -251,131 +351,147 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_addr = lane_base + t * 128;
     const uint32_t o_addr = lane_base + 256 + t * 128;
-    float m_used = -INFINITY;
-    float l = 0.f;
-    int j = 0;
     bool ok = true;
-    for (int ii = run.item_begin; ii < run.item_end && ok; ++ii) {
-      const fcp_item itm = a.items[ii];
-      const int nkt = kv_tiles(itm, qt);
-      for (int kt = 0; kt < nkt; ++kt, ++j) {
-        const int kv_valid = itm.kv_len - kt * kTileN;
-        const bool diag = itm.mask == FCP_MASK_CAUSAL_DIAG && kt == qt;
-        const int lim = diag ? min(r + 1, kv_valid) : kv_valid;  // visible key columns [0, lim)
-        ok = mbar_wait(bar(B_SFULL + t), j & 1, abort_flag, a.err, kErrFwdWait + 8);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t sv[128];
-        tmem_ld128(s_addr, sv);
-        // tiles with every column visible to every row of the warp take the short path
-        // (packed float32x2 arithmetic, 3-input max); diagonal and ragged tiles mask
-        const bool full = __all_sync(0xffffffffu, lim >= kTileN);
-        float mx;
-        if (full) {
-          float mc[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            mc[c] = __uint_as_float(sv[32 * c]);
-#pragma unroll
-            for (int e = 0; e < 15; ++e)
-              mc[c] = max3f(mc[c], __uint_as_float(sv[32 * c + 1 + 2 * e]), __uint_as_float(sv[32 * c + 2 + 2 * e]));
-            mc[c] = fmaxf(mc[c], __uint_as_float(sv[32 * c + 31]));
-          }
-          mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
-        } else {
-          mx = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (e < lim) mx = fmaxf(mx, __uint_as_float(sv[e]));
-        }
-        const float m_new = fmaxf(m_used, mx * a.scale_log2);
-        float alpha = 1.f;
-        const bool grow = m_new > m_used + kRescaleThreshold;
-        if (grow) {
-          alpha = fast_exp2(m_used - m_new);
-          m_used = m_new;
-        }
-        const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-        float rowsum = 0.f;
-        if (full) {
-          float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int i0 = 32 * c + 2 * e;
-              const float2 x = ffma2(__uint_as_float(sv[i0]), __uint_as_float(sv[i0 + 1]), a.scale_log2, a.scale_log2,
-                                     -mb, -mb);
-              const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-              acc2 = fadd2(acc2.x, acc2.y, p0, p1);
-              pk[e] = pack_bf16(p0, p1);
-            }
-            tmem_st16(s_addr + c * 16, pk);
-          }
-          rowsum = acc2.x + acc2.y;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c0 = c * 32 + 2 * e;
-              const float p0 = (c0 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0]), a.scale_log2, -mb)) : 0.f;
-              const float p1 = (c0 + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), a.scale_log2, -mb)) : 0.f;
-              rowsum += p0 + p1;
-              pk[e] = pack_bf16(p0, p1);
-            }
-            tmem_st16(s_addr + c * 16, pk);
-          }
-        }
-        l = l * alpha + rowsum;
-        // O holds the sum through key tile j-1 once PV(t, j-1) completes; rows whose maximum
-        // grew are rescaled before PV(t, j) adds onto it (warp-uniform TMEM access).
-        if (__any_sync(0xffffffffu, grow && j > 0)) {
-          ok = mbar_wait(bar(B_ODONE + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 9);
+    int J = 0;
+    for (int u = 0; ok; ++u) {
+      const Tile T = next_tile(u, kErrFwdWait + 15);
+      if (T.valid <= 0) break;
+      const int qt = T.qt;
+      float m_used = -INFINITY;
+      float l = 0.f;
+      int jl = 0;
+      for (int ii = T.item_begin; ii < T.item_end && ok; ++ii) {
+        const fcp_item itm = a.items[ii];
+        const int nkt = kv_tiles(itm, qt);
+        for (int kt = 0; kt < nkt; ++kt, ++J, ++jl) {
+          const int kv_valid = itm.kv_len - kt * kTileN;
+          const bool diag = itm.mask == FCP_MASK_CAUSAL_DIAG && kt == qt;
+          const int lim = diag ? min(r + 1, kv_valid) : kv_valid;  // visible key columns [0, lim)
+          ok = mbar_wait(bar(B_SFULL + t), J & 1, abort_flag, a.err, kErrFwdWait + 8);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
+          uint32_t sv[128];
+          tmem_ld128(s_addr, sv);
+          // tiles with every column visible to every row of the warp take the short path
+          // (packed float32x2 arithmetic, 3-input max); diagonal and ragged tiles mask
+          const bool full = __all_sync(0xffffffffu, lim >= kTileN);
+          float mx;
+          if (full) {
+            float mc[4];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(o_addr + c * 32, ov);
+            for (int c = 0; c < 4; ++c) {
+              mc[c] = __uint_as_float(sv[32 * c]);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(o_addr + c * 32, ov);
+              for (int e = 0; e < 15; ++e)
+                mc[c] = max3f(mc[c], __uint_as_float(sv[32 * c + 1 + 2 * e]), __uint_as_float(sv[32 * c + 2 + 2 * e]));
+              mc[c] = fmaxf(mc[c], __uint_as_float(sv[32 * c + 31]));
+            }
+            mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+          } else {
+            mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+              if (e < lim) mx = fmaxf(mx, __uint_as_float(sv[e]));
           }
+          const float m_new = fmaxf(m_used, mx * a.scale_log2);
+          float alpha = 1.f;
+          const bool grow = m_new > m_used + kRescaleThreshold;
+          if (grow) {
+            alpha = fast_exp2(m_used - m_new);
+            m_used = m_new;
+          }
+          const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+          float rowsum = 0.f;
+          if (full) {
+            float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int i0 = 32 * c + 2 * e;
+                const float2 x = ffma2(__uint_as_float(sv[i0]), __uint_as_float(sv[i0 + 1]), a.scale_log2,
+                                       a.scale_log2, -mb, -mb);
+                const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                acc2 = fadd2(acc2.x, acc2.y, p0, p1);
+                pk[e] = pack_bf16(p0, p1);
+              }
+              tmem_st16(s_addr + c * 16, pk);
+            }
+            rowsum = acc2.x + acc2.y;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int c0 = c * 32 + 2 * e;
+                const float p0 = (c0 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0]), a.scale_log2, -mb)) : 0.f;
+                const float p1 =
+                    (c0 + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), a.scale_log2, -mb)) : 0.f;
+                rowsum += p0 + p1;
+                pk[e] = pack_bf16(p0, p1);
+              }
+              tmem_st16(s_addr + c * 16, pk);
+            }
+          }
+          l = l * alpha + rowsum;
+          // O holds the sum through key tile jl-1 once PV(t, jl-1) completes; rows whose
+          // maximum grew are rescaled before PV(t, jl) adds onto it (warp-uniform TMEM access).
+          if (__any_sync(0xffffffffu, grow && jl > 0)) {
+            ok = mbar_wait(bar(B_ODONE + t), (J - 1) & 1, abort_flag, a.err, kErrFwdWait + 9);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(o_addr + c * 32, ov);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              tmem_st32(o_addr + c * 32, ov);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(B_PFULL + t));
         }
-        tmem_st_wait();
+      }
+      if (!ok) break;
+      if (jl == 0) {  // no key tile (not produced by the planner): O_t was never written
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL + t));
+        mbar_arrive(bar(B_OFREE + t));
+        continue;
       }
-    }
-    if (ok && j > 0) {
-      ok = mbar_wait(bar(B_ODONE + t), (j - 1) & 1, abort_flag, a.err, kErrFwdWait + 10);
+      // epilogue: O_t is read out of TMEM (then released to the next tile's first PV) and
+      // the normalised partial is stored
+      ok = mbar_wait(bar(B_ODONE + t), (J - 1) & 1, abort_flag, a.err, kErrFwdWait + 10);
       ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
-        tc_fence_after();
-        const int qrow = qt * kTileM + r;
-        const bool store = qrow < run.q_len && (t == 0 || has_h1);
-        const int h = t ? h1 : h0;
-        const long long prow = static_cast<long long>(h) * a.part_rows + run.part_row0 + qrow;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D);
+      if (!ok) break;
+      tc_fence_after();
+      const int qrow = qt * kTileM + r;
+      const bool store = qrow < T.q_len && (t == 0 || T.has_h1);
+      const int h = t ? T.h1 : T.h0;
+      const long long prow = static_cast<long long>(h) * a.part_rows + T.part_row0 + qrow;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(o_addr + c * 32, ov);
-          if (store) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[c * 8 + e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
-                                           __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
-          }
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(o_addr + c * 32, ov);
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(B_OFREE + t));
         }
-        if (store) a.part_lse[prow] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (store) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[c * 8 + e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
+                                         __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+        }
       }
+      if (store) a.part_lse[prow] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -420,8 +536,15 @@ fcp_status launch_fwd(const fcp_plan* plan, const void* d_plan, int32_t unit_beg
   a.err = dev_error_word(d_plan);
   FCP_CUDA_TRY(cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                "fwd smem attribute");
-  const long long grid = static_cast<long long>(n_units) * hkv * a.pairs_per_group;
-  if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
+  a.n_tiles = static_cast<long long>(n_units) * hkv * a.pairs_per_group;
+  a.next_tile = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(const_cast<void*>(d_plan)) +
+                                                       kDevFwdTileOffset);
+  FCP_CUDA_TRY(cudaMemsetAsync(a.next_tile, 0, sizeof(unsigned long long), stream), "fwd tile counter");
+  // persistent: one CTA per SM (the kernel holds all 512 TMEM columns), each walking tiles
+  int dev = 0, n_sm = 0;
+  FCP_CUDA_TRY(cudaGetDevice(&dev), "fwd device");
+  FCP_CUDA_TRY(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev), "fwd SM count");
+  const long long grid = std::min<long long>(a.n_tiles, std::max(n_sm, 1));
   fwd_kernel<D><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(mq, mk, mv, a);
   FCP_CUDA_TRY(cudaGetLastError(), "fwd launch");
   return FCP_OK;

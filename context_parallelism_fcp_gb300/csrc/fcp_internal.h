@@ -45,9 +45,13 @@ struct BwdUnit {
 struct DevHeader {
   int32_t error;
   int32_t error_info;
-  int32_t reserved[62];
+  int32_t reserved0[14];
+  unsigned long long fwd_next_tile;  // tile counter of the persistent forward, zeroed per launch
+  int32_t reserved[46];
 };
+constexpr size_t kDevFwdTileOffset = 64;
 static_assert(sizeof(DevHeader) == 256, "header is one 256-byte line");
+static_assert(offsetof(DevHeader, fwd_next_tile) == kDevFwdTileOffset, "tile counter offset");
 
 // Byte offsets of the arrays in the device image and their lengths.
 struct DevLayout {

@@ -210,7 +210,9 @@ fcp_status fcp_partial_sizes(const fcp_plan* plan, int32_t hq, int32_t head_dim,
  * scaled masked scores over the keys of the run's items, giving part_o[h, part_row0 + i, :]
  * (normalised over those keys) and part_lse[h, part_row0 + i] (natural log-sum-exp).
  * Inputs q, k, v bf16 device tensors as above; outputs float32 device buffers sized by
- * fcp_partial_sizes. Errors: FCP_ERR_INVALID (nulls, Hq % Hkv != 0),
+ * fcp_partial_sizes. The kernel is persistent and takes its tiles from a counter kept in
+ * d_plan (reset on `stream` before the launch), so forward launches that share one d_plan
+ * must be ordered on one stream. Errors: FCP_ERR_INVALID (nulls, Hq % Hkv != 0),
  * FCP_ERR_UNSUPPORTED (D), FCP_ERR_STATE, FCP_ERR_CUDA. */
 fcp_status fcp_block_attn_fwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
                               const void* v, int32_t hq, int32_t hkv, int32_t head_dim, float* part_o,
