@@ -39,6 +39,9 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="only the headline step (for profiling): no e2e, CPU baseline, reshuffle, sweep, "
+                         "planner comparison, solver, pipeline or balance sections")
     ap.add_argument("--block", type=int, default=HEADLINE_BLOCK)
     ap.add_argument("--coalesce", type=int, default=16)
     ap.add_argument("--seq-len", type=int, default=32768,
@@ -322,7 +325,7 @@ def bench_fcp(args):
             torch.distributed.barrier()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.step_only:
         cpu = cpu_baseline_sample(w)
 
     # warm-up, then exactly K timed steps bracketed by barrier + synchronize
@@ -395,15 +398,15 @@ def bench_fcp(args):
     result["imbalance"] = round((mx - sum(loads) / len(loads)) / mx, 6) if mx else 0.0
 
     # end to end through the public API: pinned host inputs -> device, step, results -> host
-    if not args.no_e2e:
+    if not args.no_e2e and not args.step_only:
         result["e2e"] = e2e(torch, fcp, w, args, dev, stream, step)
 
-    result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
-    if not args.no_sweep:
+    if not args.step_only:
+        result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
+    if not args.no_sweep and not args.step_only:
         result["fcp_vs_ring"] = planner_compare(torch, fcp, W, dev, stream, flush, sustained)
-    if not args.no_sweep:
         result["sweep"] = sweep(torch, fcp, W, args, dev, stream, flush, sustained)
-    if rank == 0:
+    if rank == 0 and not args.step_only:
         result["solver"] = solver_report(fcp, W)
         result["pipeline"] = pipeline_bench(torch, fcp, W, dev, stream, flush, sustained)
         result["balance"] = balance_report(W)

@@ -56,13 +56,13 @@ enum : int {
   B_VFULL = 6,
   B_VEMPTY = 8,
   B_SFULL = 10,  // per tile
-  B_PFULL = 12,  // per tile
-  B_ODONE = 14,  // per tile
-  B_OFREE = 16,  // per tile: the epilogue has read O_t out of TMEM
-  B_DRAIN = 18,
-  B_TFULL = 19,   // 2 slots: the producer has published the next tile index
-  B_TEMPTY = 21,  // 2 slots: the MMA warp and the 8 softmax warps have read it
-  B_COUNT = 23
+  B_PFULL = 12,  // per tile and half: keys [0, 64) and [64, 128) of P are in TMEM
+  B_ODONE = 16,  // per tile
+  B_OFREE = 18,  // per tile: the epilogue has read O_t out of TMEM
+  B_DRAIN = 20,
+  B_TFULL = 21,   // 2 slots: the producer has published the next tile index
+  B_TEMPTY = 23,  // 2 slots: the MMA warp and the 8 softmax warps have read it
+  B_COUNT = 25
 };
 
 // barrier area: mbarriers, abort flag, TMEM base, then the 2-slot tile ring (48 bytes a slot)
@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_PFULL + s), kTileM);
+      mbar_init(bar(B_PFULL + 2 * s), kTileM);
+      mbar_init(bar(B_PFULL + 2 * s + 1), kTileM);
       mbar_init(bar(B_ODONE + s), 1);
       mbar_init(bar(B_OFREE + s), kTileM);
     }
@@ -275,13 +276,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mma_ss_w(d, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), C::kIdescS, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int s, bool acc) {
+      // O_t += P_t V for global key tile J-1, in two halves of 64 keys: each is issued as
+      // soon as the softmax has stored that half of P
+      auto issue_pv = [&](int t, int s, bool acc, int J) -> bool {
         const uint32_t d = tmem + 256 + t * 128;
         const uint32_t p = tmem + t * 128;
         const uint32_t vbase = sb + C::kV + s * C::kTileBytes;
+        for (int half = 0; half < 2; ++half) {
+          if (!wwait(bar(B_PFULL + 2 * t + half), (J - 1) & 1, kErrFwdWait + 6)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts_w(d, p + kk * 8, sdesc_sw128(vbase + kk * 2048, kPanelBytes, 1024), C::kIdescPV, (acc || kk > 0));
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * half + k4;
+            mma_ts_w(d, p + kk * 8, sdesc_sw128(vbase + kk * 2048, kPanelBytes, 1024), C::kIdescPV,
+                     (acc || kk > 0));
+          }
+        }
+        return true;
       };
       // PV of global key tile J-1 (local index jl-1) for both heads; the first PV of a tile
       // overwrites O_t, which the previous tile's epilogue must have read out first
@@ -289,10 +300,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int ps = (J - 1) & 1;
         if (!wwait(bar(B_VFULL + ps), ((J - 1) >> 1) & 1, kErrFwdWait + 5)) return false;
         for (int t = 0; t < 2; ++t) {
-          if (!wwait(bar(B_PFULL + t), (J - 1) & 1, kErrFwdWait + 6)) return false;
           if (jl == 1 && u > 0 && !wwait(bar(B_OFREE + t), (u - 1) & 1, kErrFwdWait + 12)) return false;
-          tc_fence_after();
-          issue_pv(t, ps, jl - 1 > 0);
+          if (!issue_pv(t, ps, jl - 1 > 0, J)) return false;
           tc_commit_w(bar(B_ODONE + t));
           if (t == 1 && last) tc_commit_w(bar(B_VEMPTY + ps));
         }
@@ -319,13 +328,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               if (jl > 0) {
                 const int ps = (J - 1) & 1;
                 if (t == 0 && !wwait(bar(B_VFULL + ps), ((J - 1) >> 1) & 1, kErrFwdWait + 5)) { ok = false; break; }
-                if (!wwait(bar(B_PFULL + t), (J - 1) & 1, kErrFwdWait + 6)) { ok = false; break; }
                 if (jl == 1 && u > 0 && !wwait(bar(B_OFREE + t), (u - 1) & 1, kErrFwdWait + 12)) {
                   ok = false;
                   break;
                 }
-                tc_fence_after();
-                issue_pv(t, ps, jl - 1 > 0);
+                if (!issue_pv(t, ps, jl - 1 > 0, J)) { ok = false; break; }
                 tc_commit_w(bar(B_ODONE + t));
                 if (t == 1) tc_commit_w(bar(B_VEMPTY + ps));
               }
@@ -402,60 +409,67 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             m_used = m_new;
           }
           const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+          // P in two halves of 64 keys, each handed to the MMA warp as soon as it is stored
           float rowsum = 0.f;
-          if (full) {
-            float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t pk[16];
+          for (int half = 0; half < 2; ++half) {
+            if (full) {
+              float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int i0 = 32 * c + 2 * e;
-                const float2 x = ffma2(__uint_as_float(sv[i0]), __uint_as_float(sv[i0 + 1]), a.scale_log2,
-                                       a.scale_log2, -mb, -mb);
-                const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                acc2 = fadd2(acc2.x, acc2.y, p0, p1);
-                pk[e] = pack_bf16(p0, p1);
+              for (int c = 2 * half; c < 2 * half + 2; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const int i0 = 32 * c + 2 * e;
+                  const float2 x = ffma2(__uint_as_float(sv[i0]), __uint_as_float(sv[i0 + 1]), a.scale_log2,
+                                         a.scale_log2, -mb, -mb);
+                  const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                  acc2 = fadd2(acc2.x, acc2.y, p0, p1);
+                  pk[e] = pack_bf16(p0, p1);
+                }
+                tmem_st16(s_addr + c * 16, pk);
               }
-              tmem_st16(s_addr + c * 16, pk);
-            }
-            rowsum = acc2.x + acc2.y;
-          } else {
+              rowsum += acc2.x + acc2.y;
+            } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t pk[16];
+              for (int c = 2 * half; c < 2 * half + 2; ++c) {
+                uint32_t pk[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int c0 = c * 32 + 2 * e;
-                const float p0 = (c0 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0]), a.scale_log2, -mb)) : 0.f;
-                const float p1 =
-                    (c0 + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), a.scale_log2, -mb)) : 0.f;
-                rowsum += p0 + p1;
-                pk[e] = pack_bf16(p0, p1);
+                for (int e = 0; e < 16; ++e) {
+                  const int c0 = c * 32 + 2 * e;
+                  const float p0 = (c0 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0]), a.scale_log2, -mb)) : 0.f;
+                  const float p1 =
+                      (c0 + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c0 + 1]), a.scale_log2, -mb)) : 0.f;
+                  rowsum += p0 + p1;
+                  pk[e] = pack_bf16(p0, p1);
+                }
+                tmem_st16(s_addr + c * 16, pk);
               }
-              tmem_st16(s_addr + c * 16, pk);
             }
+            if (half == 0) {
+              // O holds the sum through key tile jl-1 once PV(t, jl-1) completes; rows whose
+              // maximum grew are rescaled before PV(t, jl) adds onto it (warp-uniform TMEM access).
+              if (__any_sync(0xffffffffu, grow && jl > 0)) {
+                ok = mbar_wait(bar(B_ODONE + t), (J - 1) & 1, abort_flag, a.err, kErrFwdWait + 9);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                  uint32_t ov[32];
+                  tmem_ld32(o_addr + c * 32, ov);
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                  tmem_st32(o_addr + c * 32, ov);
+                }
+              }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(B_PFULL + 2 * t + half));
           }
+          if (!ok) break;
           l = l * alpha + rowsum;
-          // O holds the sum through key tile jl-1 once PV(t, jl-1) completes; rows whose
-          // maximum grew are rescaled before PV(t, jl) adds onto it (warp-uniform TMEM access).
-          if (__any_sync(0xffffffffu, grow && jl > 0)) {
-            ok = mbar_wait(bar(B_ODONE + t), (J - 1) & 1, abort_flag, a.err, kErrFwdWait + 9);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t ov[32];
-              tmem_ld32(o_addr + c * 32, ov);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              tmem_st32(o_addr + c * 32, ov);
-            }
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bar(B_PFULL + t));
         }
       }
       if (!ok) break;
