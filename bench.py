@@ -341,6 +341,7 @@ def bench_fcp(args):
         raise RuntimeError(f"device error word 0x{code:x}")
 
     ms = statistics.mean(t["total"] for t in times)
+    ms_median = statistics.median(t["total"] for t in times)
     phase = {k: statistics.mean(t[k] for t in times) for k in ("fwd", "merge", "prologue", "bwd", "convert")}
     ms = max_over_ranks(ms, dev)
     value = whole_job_tflops(step.fwd_flops + step.bwd_flops, world, ms)
@@ -363,6 +364,7 @@ def bench_fcp(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 3),
+        "ms_per_step_median": round(ms_median, 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -506,21 +508,26 @@ def e2e(torch, fcp, w, args, dev, stream, step):
             "serial": {"value": round(flops / (ms_serial * 1e-3) / 1e12, 2), "ms_per_step": round(ms_serial, 3)}}
 
 
+SWEEP_RUNS = 20  # timed runs per sweep point (the median is reported)
+
+
 def sweep(torch, fcp, W, args, dev, stream, flush, sustained):
     out = []
     for b in SWEEP:
         w = W.block_sweep(b)
         for c in ((args.coalesce, 1) if b <= 1024 else (args.coalesce,)):
             st = Step(fcp, torch, w, c, dev, stream)
-            times = timed_steps(torch, st, max(3, args.steps // 2), 2, flush)
-            fwd = statistics.mean(t["fwd"] + t["merge"] for t in times)
-            bwd = statistics.mean(t["prologue"] + t["bwd"] + t["convert"] for t in times)
-            fk = statistics.mean(t["fwd"] for t in times)
-            bk = statistics.mean(t["bwd"] for t in times)
+            times = timed_steps(torch, st, SWEEP_RUNS, 3, flush)
+            # medians over the runs (each run: L2 flushed, plan rebuilt, whole step)
+            fwd = statistics.median(t["fwd"] + t["merge"] for t in times)
+            bwd = statistics.median(t["prologue"] + t["bwd"] + t["convert"] for t in times)
+            fk = statistics.median(t["fwd"] for t in times)
+            bk = statistics.median(t["bwd"] for t in times)
             ftf = st.fwd_flops / (fwd * 1e-3) / 1e12
             btf = st.bwd_flops / (bwd * 1e-3) / 1e12
             tot = (st.fwd_flops + st.bwd_flops) / ((fwd + bwd) * 1e-3) / 1e12
             out.append({"block": b, "blocks": 32768 // b, "coalesce": c, "items": st.plan.view()["n_items"],
+                        "runs_timed": len(times), "statistic": "median",
                         "fwd_tflops": round(ftf, 1), "bwd_tflops": round(btf, 1), "fwd_bwd_tflops": round(tot, 1),
                         "fwd_kernel_tflops": round(st.fwd_flops / (fk * 1e-3) / 1e12, 1),
                         "bwd_kernel_tflops": round(st.bwd_flops / (bk * 1e-3) / 1e12, 1),
