@@ -11,17 +11,19 @@
 // persistent: one CTA per SM takes tiles (sorted longest first) from a global counter, and
 // the next tile's Q load, the K/V ring and the previous tile's partial stores overlap the
 // current tile's MMAs. 10 warps:
-//   warps 0-3  softmax of tile 0: thread = query row = TMEM lane
-//   warps 4-7  softmax of tile 1
-//   warp  8    TMA producer: Q tiles once, then K and V tiles through 2-stage rings
-//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 0-3  softmax of head 0: thread = query row = TMEM lane
+//   warps 4-7  softmax of head 1
+//   warp  8    tile scheduler and TMA producer: per tile the two Q tiles, then K and V tiles
+//              through 2-stage rings counted across tiles
+//   warp  9    TMEM allocator and MMA issuer (warp-converged, one elected lane issues)
 // TMEM (512 columns x 128 lanes, fp32): S_t at columns [128t, 128t+128), O_t at
-// [256+128t, 256+128t+D). Softmax overwrites S_t's first 64 columns with P_t as packed bf16;
-// O_t += P_t V runs with A read from TMEM. Per key tile the issue order is
-// PV(0,j-1), S(0,j), PV(1,j-1), S(1,j), so the tensor core works on one tile while the other
-// tile's softmax runs. O is rescaled lazily: only when a row maximum grows by more than
-// 2^8 (in exp2 units), keeping every P <= 256; the final normalisation uses the same stale
-// maximum, so the result is exact up to rounding.
+// [256+128t, 256+128t+D). Softmax overwrites S_t's first 64 columns with P_t as packed bf16,
+// in two halves of 64 keys, each handed to the MMA warp as soon as it is stored; O_t += P_t V
+// runs with A read from TMEM. Per key tile the issue order is PV(0,j-1), S(0,j), PV(1,j-1),
+// S(1,j), so the tensor core works on one head while the other head's softmax runs. O is
+// rescaled lazily: only when a row maximum grows by more than 2^8 (in exp2 units), keeping
+// every P <= 256; the final normalisation uses the same stale maximum, so the result is
+// exact up to rounding.
 #include "fcp_cuda_util.h"
 #include "fcp_sm100.cuh"
 
