@@ -66,3 +66,35 @@ def test_causal_mixed_pipelined_sampled(fcp):
     assert r["att"].n_stages > 1
     U.sampled_forward(r, w, rows_per_seq=24)
     U.sampled_backward(r, w, rows_per_seq=12, kv_tail=64)
+
+
+def test_full_mask_pipelined_sampled(fcp):
+    """The full-mask batch (16 lognormal sequences, 65536 tokens, 1024-token blocks, 8 workers),
+    forward only, pipelined at coalesce degree 4, on sampled rows."""
+    w = W.full_mask()
+    r = U.run_path(fcp, w, pipeline=4)
+    assert r["att"].n_stages > 2
+    U.sampled_forward(r, w, rows_per_seq=24)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_plan_pipelined(fcp, causal):
+    """The ring baseline's plan also runs through the pipeline (many small blocks, many stages)."""
+    w = W.Workload("ring pipe", [1500, 40, 700, 2600], 256, 8, 2, 128, 4, causal)
+    plan = fcp.Plan.ring(w.seqlens, w.n_workers, w.causal)
+    n = plan.schedule(2)
+    assert n > 2
+    att = fcp.FcpAttention.from_plan(plan, w.hq, w.hkv, w.head_dim, backward=True)
+    assert att.n_stages == n
+    q, k, v = W.make_qkv(w, device="cuda")
+    do = W.make_dout(w, device="cuda")
+    o, lse = att.forward(q, k, v)
+    dq, dk, dv = att.backward(q, k, v, o, lse, do)
+    torch.cuda.synchronize()
+    att.check_device_error()
+    Q, K, V, dO = (U.np64(t) for t in (q, k, v, do))
+    ro, rl = A.attention_forward(Q, K, V, w.seqlens, causal)
+    U.check_forward(U.np64(o), U.np64(lse), ro, rl, "ring pipelined")
+    rdq, rdk, rdv = A.attention_backward(Q, K, V, dO, w.seqlens, causal)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), (rdq, rdk, rdv)):
+        U.check_grad(name, U.np64(got), ref, "ring pipelined")

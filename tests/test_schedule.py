@@ -286,3 +286,19 @@ def test_set_stages_rejects_invalid(fcp):
     with pytest.raises(fcp.FcpError) as e:
         undistributed.schedule(1)
     assert e.value.status == 5
+
+
+@pytest.mark.parametrize("seqlens,b,causal,n", [
+    ([0, 300, 0, 5], 64, True, 3),       # empty sequences and a packed short one
+    ([1024], 256, True, 1),               # one worker: every block local, one stage
+    ([40, 17, 3, 60], 64, False, 4),      # packed blocks only (full mask)
+    ([512, 512], 128, True, 8),           # more workers than blocks
+])
+@pytest.mark.parametrize("degree", [1, 1000])
+def test_library_schedule_edge_cases(fcp, seqlens, b, causal, n, degree):
+    plan = _lib_vs_oracle(fcp, seqlens, b, causal, n, None, degree)
+    v = plan.view()
+    if n == 1:
+        assert v["n_exec_stages"] == 1
+    if degree >= 1000:
+        assert v["n_exec_stages"] <= 2
