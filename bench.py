@@ -154,7 +154,8 @@ class Step:
         self.fcp, self.torch, self.w, self.c, self.dev, self.stream = fcp, torch, w, coalesce, device, stream
         self.planner = planner
         self.pipeline = pipeline  # coalesce degree of the block-level pipeline, or None
-        self.replan = replan  # rebuild the plan inside each step (host work in the timed region)
+        self.replan = replan  # rebuild the plan for every step (host work in the timed region)
+        self.next_plan = None
         self.q, self.k, self.v = W.make_qkv(w, device=device)
         self.do = W.make_dout(w, device=device)
         plan = self.make_plan()
@@ -202,7 +203,10 @@ class Step:
         rec = (lambda i: ev[i].record(s)) if ev is not None else (lambda i: None)
         rec(0)
         if self.replan:
-            plan = self.make_plan()  # host: partition + LPT distribute + coalesce (or schedule)
+            # the plan built while the previous step ran (partition + LPT distribute + coalesce
+            # or schedule, on the host), uploaded in stream order
+            plan = self.next_plan if self.next_plan is not None else self.make_plan()
+            self.next_plan = None
             plan.upload(self.d_plan, s)
             self.plan = plan
         plan = self.plan
@@ -222,6 +226,10 @@ class Step:
             rec(4)
             f.block_attn_bwd_dq_convert(plan, self.dq_acc, self.dq, s)
         rec(5)
+        if self.replan:
+            # the next batch's plan is built on the host while this step's kernels run, as a
+            # training loop would overlap it
+            self.next_plan = self.make_plan()
 
 
 def timed_steps(torch, step, steps, warmup, flush, backward=True):
