@@ -14,7 +14,10 @@
  *     tensors; Section 2.3: associativity, partial results over slices of L reduced
  *     to the final output (here: the log-sum-exp merge).
  *   - Section 4.2 (bottom-up coalescer): c consecutive block sub-stages of a worker
- *     executed as one stage.
+ *     executed as one stage; block-level pipelining and the congestion-free solver
+ *     (the transfers of remote KV blocks split into Delta matchings).
+ *   - Section 4.3 (transparent reshuffler): the permutation between the user's token
+ *     order and the workers' order.
  *
  * Conventions for every call:
  *   - Device tensors are packed over tokens in input order: Q, O, dO, dQ are
@@ -142,8 +145,9 @@ fcp_status fcp_partition_ring(const int32_t* seqlens, int32_t n_seqs, int32_t n_
 
 /* Bottom-up coalescing (Section 4.2): rebuild runs so that up to `degree` consecutive
  * items of one worker over the same query range share one partial result. degree = 1
- * gives one partial per (Q-block, KV-block) pair. Errors: FCP_ERR_INVALID (degree <= 0),
- * FCP_ERR_STATE (not distributed). */
+ * gives one partial per (Q-block, KV-block) pair. A plan that fcp_schedule ordered returns
+ * to the work-list order first. Errors: FCP_ERR_INVALID (degree <= 0), FCP_ERR_STATE (not
+ * distributed). */
 fcp_status fcp_coalesce(fcp_plan* plan, int32_t degree);
 
 /* Congestion-free solver (Section 4.2, "Congestion-free solver"; Lemmas 1 and 2; Figure 8):
@@ -164,7 +168,8 @@ fcp_status fcp_solve_stages(fcp_plan* plan);
  * number of edges; every sub-stage must be a matching (each worker sends at most one block
  * and receives at most one), each in [0, 2^24). The number of sub-stages becomes
  * max(stages) + 1, which may exceed Delta. Errors: FCP_ERR_INVALID (count mismatch, a stage
- * out of range, a sub-stage that is not a matching; the plan is left unsolved), FCP_ERR_STATE (not distributed). */
+ * out of range, a sub-stage that is not a matching; the plan is left unsolved),
+ * FCP_ERR_STATE (not distributed). */
 fcp_status fcp_set_stages(fcp_plan* plan, const int32_t* stages, int32_t n_transfers);
 
 /* Read-only access to the solver's result: *transfers (n_transfers entries, valid until
