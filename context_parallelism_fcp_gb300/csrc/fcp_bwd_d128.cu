@@ -126,18 +126,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(B_KVFULL), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(B_QFULL + s), 32);
+      mbar_init(bar(B_QFULL + s), 1);
       mbar_init(bar(B_QEMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_STFULL + b), 1);
-      mbar_init(bar(B_DSFULL + b), 256);
+      mbar_init(bar(B_DSFULL + b), 8);
       mbar_init(bar(B_DSEMPTY + b), 1);
       mbar_init(bar(B_DQFULL + b), 1);
-      mbar_init(bar(B_DQEMPTY + b), 128);
+      mbar_init(bar(B_DQEMPTY + b), 4);
     }
     mbar_init(bar(B_ACCDONE), 1);
-    mbar_init(bar(B_STGFULL), 128);
+    mbar_init(bar(B_STGFULL), 4);
     mbar_init(bar(B_STGFREE), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
     mbar_fence_init();
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[c] = in ? a.lse[rowbase + c] * 1.4426950408889634f : INFINITY;
           v[kBQ + c] = in ? a.di[rowbase + c] : 0.f;
         }
-        mbar_arrive(bar(B_QFULL + s));
+        mbar_arrive_warp(bar(B_QFULL + s));
         return true;
       });
     }
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(B_DSFULL + b));
+        mbar_arrive_warp(bar(B_DSFULL + b));
         return true;
       });
     }
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t x0[32], x1[32];
         tmem_ld32x2(lane_base + 128 * b + 64, lane_base + 128 * b + 96, x0, x1);
         tc_fence_before();
-        mbar_arrive(bar(B_DQEMPTY + b));  // TMEM buffer free
+        mbar_arrive_warp(bar(B_DQEMPTY + b));  // TMEM buffer free
         // the staging tile is free once the previous step's reduce has read it
         ok = mbar_wait(bar(B_STGFREE), (step & 1) ^ 1, abort_flag, a.err, kErrBwdWait + 12);
         ok = __all_sync(0xffffffffu, ok);
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 32; ++q) stage[(32 + q) * kD + d] = __uint_as_float(x1[q]);
         fence_proxy_async_smem();
-        mbar_arrive(bar(B_STGFULL));
+        mbar_arrive_warp(bar(B_STGFULL));
         if (issuer) {
           ok = mbar_wait(bar(B_STGFULL), step & 1, abort_flag, a.err, kErrBwdWait + 13);
           if (ok) {

@@ -174,10 +174,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_PFULL + 2 * s), kTileM);
-      mbar_init(bar(B_PFULL + 2 * s + 1), kTileM);
+      mbar_init(bar(B_PFULL + 2 * s), 4);  // one arrival per softmax warp of the head
+      mbar_init(bar(B_PFULL + 2 * s + 1), 4);
       mbar_init(bar(B_ODONE + s), 1);
-      mbar_init(bar(B_OFREE + s), kTileM);
+      mbar_init(bar(B_OFREE + s), 4);
     }
     mbar_init(bar(B_DRAIN), 1);
     for (int k = 0; k < 2; ++k) {
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL + 2 * t + half));
+            mbar_arrive_warp(bar(B_PFULL + 2 * t + half));
           }
           if (!ok) break;
           l = l * alpha + rowsum;
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok) break;
       if (jl == 0) {  // no key tile (not produced by the planner): O_t was never written
         tc_fence_before();
-        mbar_arrive(bar(B_OFREE + t));
+        mbar_arrive_warp(bar(B_OFREE + t));
         continue;
       }
       // epilogue: O_t is read out of TMEM (then released to the next tile's first PV) and
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld32(o_addr + c * 32, ov);
         if (c == D / 32 - 1) {
           tc_fence_before();
-          mbar_arrive(bar(B_OFREE + t));
+          mbar_arrive_warp(bar(B_OFREE + t));
         }
         if (store) {
 #pragma unroll

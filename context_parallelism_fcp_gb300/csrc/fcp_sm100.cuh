@@ -60,6 +60,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait until the phase of `bar` with the given parity has completed. Gives up (returns
 // false) when the CTA's abort flag is raised by another thread, or after kWaitLimitNs, in
 // which case it raises the abort flag and records `code` in *err (first error wins).
+// One arrival for the whole warp: the warp barrier orders every lane's earlier writes (and
+// fences) before lane 0's release-arrive, so the mbarrier counts warps, not threads, and the
+// 32-way same-address arrive is avoided. All lanes of the warp must call it.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
                                           int code) {
   if (mbar_try_wait(bar, parity)) return true;
