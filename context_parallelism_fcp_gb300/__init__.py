@@ -112,6 +112,7 @@ _SIGNATURES = {
     "fcp_coalesce": (_ST, [_P, _I32]),
     "fcp_schedule": (_ST, [_P, _I32, ctypes.POINTER(_I32)]),
     "fcp_plan_query": (_ST, [_P, ctypes.POINTER(_View)]),
+    "fcp_plan_validate": (_ST, [_P]),
     "fcp_solve_stages": (_ST, [_P]),
     "fcp_set_stages": (_ST, [_P, ctypes.POINTER(_I32), _I32]),
     "fcp_plan_transfers": (_ST, [_P, ctypes.POINTER(ctypes.POINTER(_Transfer)), ctypes.POINTER(_I32),
@@ -274,6 +275,12 @@ class Plan:
             out["load"] = _arr(v.worker_load, v.n_workers, None)
             out["tokens"] = _arr(v.worker_tokens, v.n_workers, None)
         return out
+
+    def validate(self) -> "Plan":
+        """Check every index of the plan and its device image (fcp_plan_validate); raises
+        FcpError naming the first violation."""
+        _check(lib().fcp_plan_validate(self._h), "fcp_plan_validate")
+        return self
 
     def device_bytes(self) -> int:
         return int(lib().fcp_plan_device_bytes(self._h))

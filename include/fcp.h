@@ -192,6 +192,16 @@ fcp_status fcp_schedule(fcp_plan* plan, int32_t degree, int32_t* n_stages);
  * place when it is called; after fcp_solve_stages or fcp_set_stages, call it again.
  * fcp_coalesce returns the plan to the unscheduled work-list order.) */
 
+/* Host-side check of a distributed plan and its device image (no counterpart on the pages;
+ * the defence that stands in for a device-side bounds checker): every item's query and key
+ * ranges lie inside [0, T) and inside one sequence; a causal item pairs a block with itself
+ * or with an earlier block; the items' unmasked pairs add up to the batch's; runs cover the
+ * work list with disjoint partial rows inside the partial buffer; every token's partial
+ * records, the forward units (per execution stage), the reversed work list, the backward
+ * units and the workers' token order are complete and in range. FCP_OK, or FCP_ERR_STATE
+ * with the first violation in fcp_last_error(). Plans built by this library always pass. */
+fcp_status fcp_plan_validate(const fcp_plan* plan);
+
 /* Fill *view with read-only pointers into the plan. */
 fcp_status fcp_plan_query(const fcp_plan* plan, fcp_plan_view* view);
 

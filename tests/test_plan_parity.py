@@ -46,6 +46,7 @@ def _compare(fcp, seqlens, b, causal, n, cap=None, c=1):
         assert np.array_equal(v["item_run"], want_run)
     assert v["partial_rows"] == sum(r[3] for r in runs)
     assert v["total_pairs"] == sum(L * (L + 1) // 2 if causal else L * L for L in seqlens)
+    plan.validate()
     return v
 
 
@@ -165,7 +166,7 @@ def test_ring_plan_bit_exact(fcp, seed):
     causal = r.random() < 0.6
     part = P.partition_ring(seqlens, n, causal)
     dist = P.distribute_fixed(part, part["owner"], n)
-    plan = fcp.Plan.ring(seqlens, n, causal)
+    plan = fcp.Plan.ring(seqlens, n, causal).validate()
     v = plan.view()
     assert v["n_blocks"] == len(part["blocks"])
     if part["blocks"]:
@@ -179,3 +180,17 @@ def test_ring_plan_bit_exact(fcp, seed):
     res = plan.solve()
     edges = P.transfers(part, dist)
     assert res["n_stages"] == P.max_degree(edges, n)
+
+
+def test_validate_cluster_plan_and_state_errors(fcp):
+    """The validator accepts the cluster-scale plan (256 workers x 32K tokens) in every form the
+    library builds (distributed, coalesced, scheduled), and refuses an undistributed plan."""
+    w = W.cluster_batch()
+    plan = fcp.Plan(w.seqlens, w.block_size, w.causal)
+    with pytest.raises(fcp.FcpError) as e:
+        plan.validate()
+    assert e.value.status == 5 and "not distributed" in str(e.value) + fcp.lib().fcp_last_error().decode()
+    plan.distribute(w.n_workers).validate()
+    plan.coalesce(16).validate()
+    plan.schedule(16)
+    plan.validate()

@@ -214,6 +214,7 @@ def _lib_vs_oracle(fcp, seqlens, b, causal, n, cap, degree):
     assert np.array_equal(v["items"], np.array(want["items"], dtype=np.int64).reshape(-1, 8))
     assert np.array_equal(v["runs"], np.array(want["runs"], dtype=np.int64).reshape(-1, 8))
     assert v["partial_rows"] == want["partial_rows"]
+    plan.validate()
     return plan
 
 
@@ -254,6 +255,7 @@ def test_library_schedule_with_its_own_solver(fcp, make, degree):
         else 1 + arrive[(int(base["items"][i][2]), int(base["items"][i][0]))] // degree), i))
     assert np.array_equal(items, base["items"][key])
     assert all(stage[r[4]:r[5]].min() == stage[r[4]:r[5]].max() == r[7] for r in v["runs"])
+    plan.validate()
     # the stage-ordered forward units: unscheduling restores the work list
     plan.coalesce(1)
     assert np.array_equal(plan.view()["items"], base["items"])
