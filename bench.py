@@ -360,7 +360,7 @@ def bench_fcp(args):
     dominant = "bwd" if phase["bwd"] >= phase["fwd"] else "fwd"
     dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
     dom_flops = step.bwd_flops if dominant == "bwd" else step.fwd_flops
-    traffic = traffic_from_profile("bwd_d128_kernel" if dominant == "bwd" else "fwd_kernel", w.block_size) \
+    traffic = traffic_from_profile("bwd_tile_kernel" if dominant == "bwd" else "fwd_kernel", w.block_size) \
         if w.head_dim == 128 and args.seq_len == 32768 else None
     merge_gbs = step.merge_bytes / (phase["merge"] * 1e-3) / 1e9
 

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfcp.so")
 
-SOURCES = ["fcp_plan.cpp", "fcp_solver.cpp", "fcp_validate.cpp", "fcp_fwd.cu", "fcp_bwd.cu", "fcp_bwd_d128.cu", "fcp_merge.cu"]
+SOURCES = ["fcp_plan.cpp", "fcp_solver.cpp", "fcp_validate.cpp", "fcp_fwd.cu", "fcp_bwd.cu", "fcp_bwd_tile.cu", "fcp_merge.cu"]
 HEADERS = ["fcp_internal.h", "fcp_cuda_util.h", "fcp_sm100.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", INCLUDE,

@@ -1,30 +1,30 @@
-// Backward block attention for head_dim 128 on sm_103a: a pipelined tile kernel.
+// Backward block attention on sm_103a (head_dim 64 or 128): a pipelined tile kernel.
 //
-// Same mathematics and work decomposition as the generic backward kernel (the exact gradient
-// of the attention of "Unleashing Scalable Context Parallelism for Foundation Models
-// Pre-Training via FCP", Section 2.2, over the reversed work list): one CTA owns a 128-row
-// key tile of one key range and one KV head, and walks every (query head of the group, item
-// reading this key range, query step) accumulating dK and dV in TMEM.
+// The exact gradient of the attention of "Unleashing Scalable Context Parallelism for
+// Foundation Models Pre-Training via FCP" (Section 2.2) over the reversed work list: one CTA
+// owns a 128-row key tile of one key range and one KV head, and walks every (query head of
+// the group, item reading this key range, query step) accumulating dK and dV in TMEM.
 //
-// What differs is the schedule. A query step is 64 rows, so the S^T/dP^T accumulators of a
-// step need 128 TMEM columns and two steps fit beside dV and dK:
+// A query step is 64 rows, so the S^T/dP^T accumulators of a step need 128 TMEM columns and
+// two steps fit beside dV and dK:
 //   columns [128b, 128b+64)     S^T of buffer b (b = step & 1); P^T (bf16) overwrites
 //                               [128b+16, 128b+48)
 //   columns [128b+64, 128b+128) dP^T; dS^T (bf16) overwrites [128b+80, 128b+112); later
 //                               dQ^T = K^T dS^T (128 lanes = channels x 64 queries)
-//   columns [256, 384) dV, [384, 512) dK
+//   columns [256, 256+D) dV, [384, 384+D) dK
 // Each gradient warpgroup reads 32 columns of S^T and of dP^T and writes its packed half of
 // P^T and dS^T inside the columns it has itself just read, so the two warpgroups never
 // need to wait for each other. S^T of step i+2 may be issued before the drain of step i
 // has read dQ^T (they occupy different halves of the buffer); only dP^T waits for it.
 // The MMA warp issues S^T/dP^T of step i+1 before it waits for the gradient warps of step
 // i, so the tensor core works on the next step while the current one is turned into P and
-// dS. dQ^T is computed with the channels on TMEM lanes, so the drain warps add it to the
-// float32 accumulator with one coalesced 128-byte atomic line per warp instruction, and free
-// the TMEM buffer as soon as the values are in registers.
+// dS. dQ^T is computed with the channels on TMEM lanes (M = 128: for D = 64 the upper 64
+// channels read a zero panel and are never drained), so the drain warps stage it in shared
+// memory with one 128-byte line per warp store and add it to the float32 accumulator with
+// one TMA reduce per step, freeing the TMEM buffer as soon as the values are in registers.
 // Warps: 0-7 gradient (two warpgroups, 32 query columns each; thread = key row = TMEM lane),
-// 8-11 dQ drain (thread = channel = TMEM lane), 12 TMA producer (Q/dO/LSE/Di, 3 stages),
-// 13 TMEM allocator and single-thread MMA issuer.
+// 8-11 dQ drain (thread = channel = TMEM lane; D/32 of them active), 12 TMA producer
+// (Q/dO/LSE/Di, 3 stages), 13 TMEM allocator and MMA issuer (warp-converged).
 #include "fcp_cuda_util.h"
 #include "fcp_sm100.cuh"
 
@@ -33,28 +33,38 @@ namespace {
 
 using namespace dev;
 
-constexpr int kD = 128;
 constexpr int kBN = 128;  // key rows per CTA
 constexpr int kBQ = 64;   // query rows per step
 constexpr int kStages = 3;
 constexpr int kThreads = 448;
 
-constexpr int kKVTile = kBN * kD * 2;      // 32768: 2 panels of [128 rows][64 ch]
-constexpr int kKVPanel = kBN * 128;        // 16384
-constexpr int kQTile = kBQ * kD * 2;       // 16384: 2 panels of [64 rows][64 ch]
-constexpr int kQPanel = kBQ * 128;         // 8192
+constexpr int kKVPanel = kBN * 128;        // 16384: [128 rows][64 ch]
+constexpr int kQPanel = kBQ * 128;         // 8192: [64 rows][64 ch]
 constexpr int kDSTile = kBN * kBQ * 2;     // 16384: [128 kv rows][64 q] bf16, one panel
 
-constexpr int kOffK = 0;
-constexpr int kOffV = kKVTile;
-constexpr int kOffQ = 2 * kKVTile;                          // kStages tiles
-constexpr int kOffDO = kOffQ + kStages * kQTile;            // kStages tiles
-constexpr int kOffDS = kOffDO + kStages * kQTile;           // 2 buffers
-constexpr int kOffVec = kOffDS + 2 * kDSTile;               // kStages x (lse2[64], di[64])
-constexpr int kOffStage = ((kOffVec + kStages * 2 * kBQ * 4) + 1023) & ~1023;  // dQ [64 q][128 d] float32
-constexpr int kStageBytes = kBQ * kD * 4;
-constexpr int kOffBar = kOffStage + kStageBytes;
-constexpr int kSmemBytes = kOffBar + 256;
+// Shared-memory layout for head dimension D. The K region always holds two panels: the
+// channels of K, then (D = 64) a zero panel, so that dQ^T = K^T dS^T is one M = 128
+// instruction for either D.
+template <int D>
+struct TileCfg {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kQTile = kBQ * D * 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = 2 * kKVPanel;
+  static constexpr int kOffQ = kOffV + kPanels * kKVPanel;   // kStages tiles
+  static constexpr int kOffDO = kOffQ + kStages * kQTile;    // kStages tiles
+  static constexpr int kOffDS = kOffDO + kStages * kQTile;   // 2 buffers
+  static constexpr int kOffVec = kOffDS + 2 * kDSTile;       // kStages x (lse2[64], di[64])
+  static constexpr int kOffStage = ((kOffVec + kStages * 2 * kBQ * 4) + 1023) & ~1023;  // dQ [64 q][D] float32
+  static constexpr int kStageBytes = kBQ * D * 4;
+  static constexpr int kOffBar = kOffStage + kStageBytes;
+  static constexpr int kSmemBytes = kOffBar + 256;
+  static constexpr int kDrainWarps = D / 32;  // drain warps holding real channels
+  // dV, dK: M = 128 keys, N = D channels, A from TMEM, B (dO / Q) MN-major.
+  static constexpr uint32_t kIdescAcc = idesc_bf16(kBN, D, false, true);
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
+  static_assert(kOffVec + kStages * 2 * kBQ * 4 <= kOffStage, "vector area");
+};
 
 // mbarrier indices, laid out from the stage count so that no two ever share a slot
 enum : int {
@@ -72,15 +82,11 @@ enum : int {
   B_COUNT = B_STGFREE + 1
 };
 static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
-static_assert(kOffVec + kStages * 2 * kBQ * 4 <= kOffStage, "vector area");
-static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // S^T, dP^T: M = 128 keys, N = 64 queries, both operands K-major.
 constexpr uint32_t kIdescST = idesc_bf16(kBN, kBQ, false, false);
-// dV, dK: M = 128 keys, N = 128 channels, A from TMEM, B (dO / Q) MN-major.
-constexpr uint32_t kIdescAcc = idesc_bf16(kBN, kD, false, true);
 // dQ^T = K^T dS^T: M = 128 channels, N = 64 queries, A (K read transposed) and B MN-major.
-constexpr uint32_t kIdescDQ = idesc_bf16(kD, kBQ, true, true);
+constexpr uint32_t kIdescDQ = idesc_bf16(128, kBQ, true, true);
 
 struct Args {
   const fcp_item* items;
@@ -98,10 +104,15 @@ struct Args {
   int* err;
 };
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_d128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    bwd_tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmDQ, const Args a) {
+  using C = TileCfg<D>;
+  constexpr int kD = D;
+  constexpr int kOffK = C::kOffK, kOffV = C::kOffV, kOffQ = C::kOffQ, kOffDO = C::kOffDO, kOffDS = C::kOffDS;
+  constexpr int kOffVec = C::kOffVec, kOffStage = C::kOffStage, kOffBar = C::kOffBar, kQTile = C::kQTile;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) atomicCAS(a.err, 0, kErrSmemAlign);
@@ -134,10 +145,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_DSFULL + b), 8);
       mbar_init(bar(B_DSEMPTY + b), 1);
       mbar_init(bar(B_DQFULL + b), 1);
-      mbar_init(bar(B_DQEMPTY + b), 4);
+      mbar_init(bar(B_DQEMPTY + b), C::kDrainWarps);
     }
     mbar_init(bar(B_ACCDONE), 1);
-    mbar_init(bar(B_STGFULL), 4);
+    mbar_init(bar(B_STGFULL), C::kDrainWarps);
     mbar_init(bar(B_STGFREE), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
     mbar_fence_init();
@@ -145,6 +156,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
+  }
+  if constexpr (D < 128) {  // the zero panel beside K's channels (read as K^T rows D..127)
+    uint4* zero = reinterpret_cast<uint4*>(smem + kOffK + C::kPanels * kKVPanel);
+    for (int i = threadIdx.x; i < (2 - C::kPanels) * kKVPanel / 16; i += kThreads) zero[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -179,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(bar(B_KVFULL), 2 * kKVTile);
+      mbar_arrive_expect_tx(bar(B_KVFULL), 2 * C::kPanels * kKVPanel);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
+      for (int p = 0; p < C::kPanels; ++p) {
         tma_load_3d(sb + kOffK + p * kKVPanel, &tmK, bar(B_KVFULL), p * 64, kv_row0, kvh);
         tma_load_3d(sb + kOffV + p * kKVPanel, &tmV, bar(B_KVFULL), p * 64, kv_row0, kvh);
       }
@@ -198,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_expect_tx(bar(B_QFULL + s), 2 * kQTile);
 #pragma unroll
-          for (int p = 0; p < 2; ++p) {
+          for (int p = 0; p < C::kPanels; ++p) {
             tma_load_3d(sb + kOffQ + s * kQTile + p * kQPanel, &tmQ, bar(B_QFULL + s), p * 64, qrow0, h);
             tma_load_3d(sb + kOffDO + s * kQTile + p * kQPanel, &tmDO, bar(B_QFULL + s), p * 64, qrow0, h);
           }
@@ -270,11 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dV += P^T dO and dK += dS^T Q: K = 64 queries in 4 steps of 16 (8 TMEM columns)
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts_w(t_dv, tmem + 128 * b + 16 + kk * 8, sdesc_sw128(db + kk * 2048, kQPanel, 1024), kIdescAcc,
+          mma_ts_w(t_dv, tmem + 128 * b + 16 + kk * 8, sdesc_sw128(db + kk * 2048, kQPanel, 1024), C::kIdescAcc,
                  (i > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts_w(t_dk, tmem + 128 * b + 80 + kk * 8, sdesc_sw128(qb + kk * 2048, kQPanel, 1024), kIdescAcc,
+          mma_ts_w(t_dk, tmem + 128 * b + 80 + kk * 8, sdesc_sw128(qb + kk * 2048, kQPanel, 1024), C::kIdescAcc,
                  (i > 0 || kk > 0));
         // dQ^T = K^T dS^T: K = 128 keys in 8 steps of 16 rows (2048 bytes)
         const uint32_t dsb = sb + kOffDS + b * kDSTile;
@@ -405,9 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    // ---------------------------------------------------------------- dQ drain (warps 8-11)
-    // dQ^T (lane = channel) goes into a [64 q][128 d] float32 staging tile; one lane adds the
+  } else if (warp - 8 < C::kDrainWarps) {
+    // ---------------------------------------------------------------- dQ drain (warps 8..)
+    // dQ^T (lane = channel) goes into a [64 q][D] float32 staging tile; one lane adds the
     // tile to the accumulator with a TMA reduce. Query rows past the item's range carry exact
     // zeros (their P and dS are 0), and rows past T are clipped by the tensor map.
     bool ok = !skip;
@@ -464,22 +480,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-// Launch of the head_dim-128 backward tile kernel (same contract as fcp_block_attn_bwd_tiles).
-fcp_status launch_bwd_d128(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
+// Launch of the backward tile kernel (same contract as fcp_block_attn_bwd_tiles).
+template <int D>
+fcp_status launch_bwd_tile(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
                            const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
                            int hq, int hkv, cudaStream_t stream) {
+  using C = TileCfg<D>;
   const DevLayout& L = plan->layout;
   if (L.n_bwd_units == 0) return FCP_OK;
   const int64_t T = plan->total_tokens;
   CUtensorMap mq, mk, mv, mdo, mdq;
   fcp_status st;
-  if ((st = make_f32x128_map(&mdq, dq_acc, hq, T, kBQ)) != FCP_OK) return st;
-  if ((st = make_bf16_map(&mq, q, hq, T, kD, kBQ)) != FCP_OK) return st;
-  if ((st = make_bf16_map(&mk, k, hkv, T, kD, kBN)) != FCP_OK) return st;
-  if ((st = make_bf16_map(&mv, v, hkv, T, kD, kBN)) != FCP_OK) return st;
-  if ((st = make_bf16_map(&mdo, dout, hq, T, kD, kBQ)) != FCP_OK) return st;
+  if ((st = make_f32_map(&mdq, dq_acc, hq, T, D, kBQ)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mq, q, hq, T, D, kBQ)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mk, k, hkv, T, D, kBN)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mv, v, hkv, T, D, kBN)) != FCP_OK) return st;
+  if ((st = make_bf16_map(&mdo, dout, hq, T, D, kBQ)) != FCP_OK) return st;
   Args a;
   a.items = dev_array<fcp_item>(d_plan, L.items);
   a.kvsegs = dev_array<KvSeg>(d_plan, L.kvsegs);
@@ -493,16 +509,26 @@ fcp_status launch_bwd_d128(const fcp_plan* plan, const void* d_plan, const void*
   a.T = T;
   a.hkv = hkv;
   a.group = hq / hkv;
-  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD)));
-  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   a.err = dev_error_word(d_plan);
-  FCP_CUDA_TRY(cudaFuncSetAttribute(bwd_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
-               "bwd d128 smem attribute");
+  FCP_CUDA_TRY(cudaFuncSetAttribute(bwd_tile_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
+               "bwd smem attribute");
   const long long grid = static_cast<long long>(L.n_bwd_units) * hkv;
   if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
-  bwd_d128_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
-  FCP_CUDA_TRY(cudaGetLastError(), "bwd d128 launch");
+  bwd_tile_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
+  FCP_CUDA_TRY(cudaGetLastError(), "bwd launch");
   return FCP_OK;
+}
+
+}  // namespace
+
+fcp_status launch_bwd_tiles(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
+                            const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
+                            int hq, int hkv, int head_dim, cudaStream_t stream) {
+  if (head_dim == 128)
+    return launch_bwd_tile<128>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, stream);
+  return launch_bwd_tile<64>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, stream);
 }
 
 }  // namespace fcp

@@ -64,15 +64,17 @@ inline fcp_status make_bf16_map(CUtensorMap* map, const void* base, int heads, i
 
 // Tensor map over a contiguous float32 tensor [heads, T, 128] with box {128, rows, 1}, no
 // swizzle: one box is `rows` tokens x 128 channels (512 bytes per row).
-inline fcp_status make_f32x128_map(CUtensorMap* map, const void* base, int heads, int64_t T, int rows) {
+// Float32 [heads, T, D] tensor (D innermost), boxes of D x rows, no swizzle (the dQ
+// accumulator that the backward's reduce-adds target).
+inline fcp_status make_f32_map(CUtensorMap* map, const void* base, int heads, int64_t T, int D, int rows) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) {
     set_last_error("cuTensorMapEncodeTiled unavailable from the driver");
     return FCP_ERR_CUDA;
   }
-  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {128 * 4, static_cast<cuuint64_t>(T) * 128 * 4};
-  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(T) * D * 4};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
