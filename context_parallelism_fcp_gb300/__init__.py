@@ -131,6 +131,7 @@ _SIGNATURES = {
     "fcp_bwd_static_scratch_bytes": (_SZ, []),
     "fcp_block_attn_bwd_static_scratch": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "fcp_reshuffle": (_ST, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
+    "fcp_selftest_bounded_wait": (_ST, [_P, _P]),
     "fcp_device_error": (_ST, [_P, ctypes.POINTER(_I32), _P]),
     "fcp_plan_free": (None, [_P]),
     "fcp_status_string": (ctypes.c_char_p, [_ST]),
@@ -434,6 +435,11 @@ def reshuffle(plan: Plan, d_plan, src, dst, to_workers: bool = True, stream=None
     row_bytes = src[0, 0].numel() * src.element_size() if src.shape[1] else 16
     _check(lib().fcp_reshuffle(plan.handle, _ptr(d_plan), _ptr(src), _ptr(dst), heads, row_bytes,
                                0 if to_workers else 1, _stream(stream)), "fcp_reshuffle")
+
+
+def selftest_bounded_wait(d_plan, stream=None) -> None:
+    """Launch the bounded-wait self-test into d_plan's error word (fcp_selftest_bounded_wait)."""
+    _check(lib().fcp_selftest_bounded_wait(_ptr(d_plan), _stream(stream)), "fcp_selftest_bounded_wait")
 
 
 def device_error(d_plan, stream=None) -> int:

@@ -12,6 +12,7 @@
 #include <cmath>
 
 #include "fcp_cuda_util.h"
+#include "fcp_sm100.cuh"
 
 namespace fcp {
 namespace {
@@ -344,6 +345,26 @@ fcp_status launch_prologue(int64_t T, const void* o, const void* dout, int hq, i
 
 using namespace fcp;
 
+namespace fcp {
+namespace {
+
+// One thread waits, with the kernels' bounded mbarrier wait, on a barrier that nothing ever
+// completes; after the wait's limit it raises the abort flag and records kErrSelfTest.
+__global__ void bounded_wait_selftest_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    dev::mbar_init(dev::smem_u32(&bar), 1);
+    abort_flag = 0;
+    dev::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) dev::mbar_wait(dev::smem_u32(&bar), 0, &abort_flag, err, kErrSelfTest);
+}
+
+}  // namespace
+}  // namespace fcp
+
 extern "C" {
 
 fcp_status fcp_plan_upload(const fcp_plan* plan, void* d_plan, size_t bytes, void* stream) {
@@ -353,6 +374,14 @@ fcp_status fcp_plan_upload(const fcp_plan* plan, void* d_plan, size_t bytes, voi
   FCP_CUDA_TRY(cudaMemcpyAsync(d_plan, plan->image.data(), plan->layout.total, cudaMemcpyHostToDevice,
                                static_cast<cudaStream_t>(stream)),
                "plan upload");
+  return FCP_OK;
+}
+
+fcp_status fcp_selftest_bounded_wait(void* d_plan, void* stream) {
+  if (d_plan == nullptr || (reinterpret_cast<uintptr_t>(d_plan) & 255u) != 0) return FCP_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fcp::bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(fcp::dev_error_word(d_plan));
+  FCP_CUDA_TRY(cudaGetLastError(), "bounded-wait self-test launch");
   return FCP_OK;
 }
 

@@ -316,6 +316,14 @@ fcp_status fcp_reshuffle(const fcp_plan* plan, const void* d_plan, const void* s
  * kernel and wait that gave up) and clear it. Returns FCP_ERR_DEVICE if it was set. */
 fcp_status fcp_device_error(const void* d_plan, int32_t* code, void* stream);
 
+/* Self-test of the device-side failure path (no counterpart on the pages): one thread waits,
+ * with the bounded mbarrier wait every tile kernel uses, on a barrier that nothing ever
+ * completes. After the wait's 2-second limit it records code 0x40 in the error word of
+ * d_plan (a device buffer of at least 256 bytes, 256-byte aligned, whose error word should
+ * be clear) and the kernel exits; the context stays usable. Read the result with
+ * fcp_device_error. Errors: FCP_ERR_INVALID, FCP_ERR_CUDA. */
+fcp_status fcp_selftest_bounded_wait(void* d_plan, void* stream);
+
 void fcp_plan_free(fcp_plan* plan);
 const char* fcp_status_string(fcp_status status);
 /* Detail of the last FCP_ERR_CUDA in this thread ("" if none). */
