@@ -390,7 +390,7 @@ def bench_fcp(args):
         "fwd_bwd_frac_of_peak": round(value / world / sustained, 4),
         "phase_ms": {k: round(v, 4) for k, v in phase.items()},
         "phase_share": {k: round(v, 4) for k, v in shares.items()},
-        "roofline": {"kernel": f"{dominant}_kernel", "bound": "tensor", "achieved": round(dom_tf, 2),
+        "roofline": {"kernel": f"{'bwd_tile_kernel' if dominant == 'bwd' else 'fwd_kernel'}<{w.head_dim}>", "bound": "tensor", "achieved": round(dom_tf, 2),
                      "peak": sustained, "unit": "TFLOP/s", "frac": round(dom_tf / sustained, 4),
                      "traffic": traffic, "algorithmic_flops_per_launch": dom_flops,
                      "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a multi-second loop)"},
