@@ -122,6 +122,20 @@ def test_edge_cases(fcp):
             U.check_grad(name, U.np64(got), ref, str(seqlens))
 
 
+@pytest.mark.parametrize("hq,hkv,head_dim", [(6, 2, 64), (6, 2, 128), (5, 1, 128), (1, 1, 64)],
+                         ids=["group3 d64", "group3 d128", "group5 d128", "one head"])
+def test_odd_head_groups(fcp, hq, hkv, head_dim):
+    """Odd group sizes leave the last head pair of a KV group with one real head (the second
+    is computed and not stored); a single head has no pair at all."""
+    w = W.Workload("odd groups", [900, 130, 2100], 512, hq, hkv, head_dim, 3, True, coalesce=2)
+    r = U.run_path(fcp, w)
+    ro, rl = A.attention_forward(r["q"], r["k"], r["v"], w.seqlens, w.causal)
+    U.check_forward(U.np64(r["o"]), U.np64(r["lse"]), ro, rl, w.name)
+    rdq, rdk, rdv = A.attention_backward(r["q"], r["k"], r["v"], r["do"], w.seqlens, w.causal)
+    for name, got, ref in zip(("dq", "dk", "dv"), r["grads"], (rdq, rdk, rdv)):
+        U.check_grad(name, U.np64(got), ref, w.name)
+
+
 def test_empty_batch_is_a_no_op(fcp):
     att = fcp.FcpAttention([0, 0], 64, True, 2, 4, 2, 64)
     q = torch.empty((4, 0, 64), dtype=torch.bfloat16, device="cuda")
