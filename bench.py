@@ -225,6 +225,9 @@ class Step:
                                    self.dq_acc, self.dk, self.dv, s)
             rec(4)
             f.block_attn_bwd_dq_convert(plan, self.dq_acc, self.dq, s)
+        else:  # forward only: the backward phases are empty
+            rec(3)
+            rec(4)
         rec(5)
         if self.replan:
             # the next batch's plan is built on the host while this step's kernels run, as a
@@ -415,6 +418,7 @@ def bench_fcp(args):
         result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
     if not args.no_sweep and not args.step_only:
         result["fcp_vs_ring"] = planner_compare(torch, fcp, W, dev, stream, flush, sustained)
+        result["configs"] = configs_bench(torch, fcp, W, dev, stream, flush, sustained)
         result["sweep"] = sweep(torch, fcp, W, args, dev, stream, flush, sustained)
     if rank == 0 and not args.step_only:
         result["solver"] = solver_report(fcp, W)
@@ -612,6 +616,34 @@ def pipeline_bench(torch, fcp, W, dev, stream, flush, sustained):
             del st
             torch.cuda.empty_cache()
         out.append({"workload": w.name, "workers": w.n_workers, "block": w.block_size, "by_degree": rows})
+    return out
+
+
+def configs_bench(torch, fcp, W, dev, stream, flush, sustained):
+    """The other named workloads, through the same step: the full-mask batch (16 lognormal
+    sequences, 65536 tokens, 1K blocks, 8 workers; forward + merge only), the causal mixed
+    batch (lognormal lengths plus a 32K outlier, 4K blocks, 16 workers) and the 524288-token
+    causal sequence (8K blocks, 32 workers; 1 warm-up and 1 timed step: about 12 s each).
+    Coalesce degree 16; L2 flushed between steps; medians of the timed steps."""
+    out = []
+    for w, steps, warm in ((W.full_mask(), 5, 2), (W.causal_mixed(), 5, 2), (W.long_causal(), 1, 1)):
+        st = Step(fcp, torch, w, 16, dev, stream)
+        times = timed_steps(torch, st, steps, warm, flush, backward=w.backward)
+        fwd = statistics.median(t["fwd"] + t["merge"] for t in times)
+        row = {"workload": w.name, "tokens": w.total_tokens, "block": w.block_size, "workers": w.n_workers,
+               "causal": w.causal, "fwd_ms": round(fwd, 3),
+               "fwd_tflops": round(st.fwd_flops / (fwd * 1e-3) / 1e12, 1)}
+        if w.backward:
+            bwd = statistics.median(t["prologue"] + t["bwd"] + t["convert"] for t in times)
+            tot = statistics.median(t["total"] for t in times)
+            row.update({"bwd_ms": round(bwd, 3), "bwd_tflops": round(st.bwd_flops / (bwd * 1e-3) / 1e12, 1),
+                        "fwd_bwd_tflops": round((st.fwd_flops + st.bwd_flops) / (tot * 1e-3) / 1e12, 1)})
+            row["frac_of_peak"] = round(row["fwd_bwd_tflops"] / sustained, 4)
+        else:
+            row["frac_of_peak"] = round(row["fwd_tflops"] / sustained, 4)
+        out.append(row)
+        del st
+        torch.cuda.empty_cache()
     return out
 
 
