@@ -105,7 +105,14 @@ void put(std::vector<uint8_t>& img, size_t off, const std::vector<T>& v) {
 
 // Device image: header, items, runs, query ranges with their runs, token -> partial rows,
 // forward units (longest first), key ranges with their items, backward units (longest first).
-bool build_image(fcp_plan* p) {
+// Device image of a distributed plan. FCP_ERR_UNSUPPORTED if its 32-bit indices would
+// overflow, FCP_ERR_STATE if an internal invariant fails.
+fcp_status build_image(fcp_plan* p) {
+  // partial rows and item indices are 32-bit in the device image
+  if (p->partial_rows > INT32_MAX || p->items.size() > static_cast<size_t>(INT32_MAX)) {
+    set_last_error("plan too large: more than 2^31 - 1 partial rows or work items (raise the coalesce degree)");
+    return FCP_ERR_UNSUPPORTED;
+  }
   const auto ranges = runs_by_range(p->runs);
   std::vector<QSeg> qsegs;
   int32_t max_runs = 0;
@@ -115,7 +122,7 @@ bool build_image(fcp_plan* p) {
     const int32_t n = static_cast<int32_t>(rg.size());
     max_runs = std::max(max_runs, n);
     for (int32_t k = 0; k < n; ++k)
-      if (p->runs[rg[k]].part_row0 != r0.part_row0 + k * r0.q_len) return false;  // contiguous rows
+      if (p->runs[rg[k]].part_row0 != r0.part_row0 + k * r0.q_len) return FCP_ERR_STATE;  // contiguous rows
     qsegs.push_back(QSeg{r0.q_tok0, r0.q_len, n, r0.part_row0});
     for (int32_t t = 0; t < r0.q_len; ++t)
       tok2part[static_cast<size_t>(r0.q_tok0) + t] = TokPart{r0.part_row0 + t, r0.q_len, n, 0};
@@ -191,7 +198,7 @@ bool build_image(fcp_plan* p) {
       for (int32_t si = B.first_seg; si < B.first_seg + B.n_segs; ++si)
         for (int32_t t = 0; t < p->segs[si].len; ++t) worker_order.push_back(p->segs[si].tok0 + t);
     }
-  if (static_cast<int64_t>(worker_order.size()) != p->total_tokens) return false;
+  if (static_cast<int64_t>(worker_order.size()) != p->total_tokens) return FCP_ERR_STATE;
 
   DevLayout L;
   size_t off = sizeof(DevHeader);
@@ -223,7 +230,7 @@ bool build_image(fcp_plan* p) {
   L.stage_unit_begin = std::move(stage_begin);
 
   for (const TokPart& tp : tok2part)
-    if (tp.count <= 0) return false;  // every token must belong to exactly one query range
+    if (tp.count <= 0) return FCP_ERR_STATE;  // every token must belong to exactly one query range
   p->image.assign(L.total, 0);
   put(p->image, L.items, p->items);
   put(p->image, L.runs, p->runs);
@@ -235,7 +242,7 @@ bool build_image(fcp_plan* p) {
   put(p->image, L.kv_items, kv_items);
   put(p->image, L.bwd_units, bwd_units);
   p->layout = L;
-  return true;
+  return FCP_OK;
 }
 
 // Loads, tokens, work list, runs and device image of a plan whose blocks have owners.
@@ -295,9 +302,9 @@ fcp_status finish_distribution(fcp_plan* p, const std::vector<int32_t>& owner, i
   p->item_stage.clear();
   p->n_exec_stages = 1;
   build_runs(p, 1);
-  if (!build_image(p)) {
+  if (const fcp_status st = build_image(p); st != FCP_OK) {
     p->distributed = false;
-    return FCP_ERR_STATE;
+    return st;
   }
   return FCP_OK;
 }
@@ -513,9 +520,9 @@ fcp_status fcp_coalesce(fcp_plan* p, int32_t degree) {
     p->n_exec_stages = 1;
   }
   build_runs(p, degree);
-  if (!build_image(p)) {
+  if (const fcp_status st = build_image(p); st != FCP_OK) {
     p->distributed = false;
-    return FCP_ERR_STATE;
+    return st;
   }
   return FCP_OK;
 }
@@ -560,9 +567,9 @@ fcp_status fcp_schedule(fcp_plan* p, int32_t degree, int32_t* n_stages) {
   p->item_stage = std::move(item_stage);
   p->n_exec_stages = n_exec;
   build_runs(p, 0);
-  if (!build_image(p)) {
+  if (const fcp_status st = build_image(p); st != FCP_OK) {
     p->distributed = false;
-    return FCP_ERR_STATE;
+    return st;
   }
   p->coalesce = degree;
   if (n_stages != nullptr) *n_stages = n_exec;

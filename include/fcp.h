@@ -129,7 +129,9 @@ fcp_status fcp_partition(const int32_t* seqlens, int32_t n_seqs, int32_t block_s
  * unpacked causal block j of a sequence pairs with KV blocks 0..j (j: CAUSAL_DIAG, others
  * FULL), a full-mask block with every block of its sequence, a packed segment with itself.
  * Runs are rebuilt with coalesce degree 1 (one partial per item). Errors: FCP_ERR_INVALID
- * (null plan, n_workers <= 0), FCP_ERR_CAPACITY (the plan is left undistributed). */
+ * (null plan, n_workers <= 0), FCP_ERR_CAPACITY (the plan is left undistributed),
+ * FCP_ERR_UNSUPPORTED (more than 2^31 - 1 partial rows or work items; also from
+ * fcp_coalesce and fcp_schedule). */
 fcp_status fcp_distribute(fcp_plan* plan, int32_t n_workers, int64_t token_cap);
 
 /* The ring-attention baseline the pages compare against (Section 3.4, "Balance-optimized",
