@@ -42,6 +42,7 @@ def parse_args():
     ap.add_argument("--step-only", action="store_true",
                     help="only the headline step (for profiling): no e2e, CPU baseline, reshuffle, sweep, "
                          "planner comparison, solver, pipeline or balance sections")
+    ap.add_argument("--with-reshuffle", action="store_true", help="keep the reshuffle section under --step-only")
     ap.add_argument("--block", type=int, default=HEADLINE_BLOCK)
     ap.add_argument("--coalesce", type=int, default=16)
     ap.add_argument("--seq-len", type=int, default=32768,
@@ -414,7 +415,7 @@ def bench_fcp(args):
     if not args.no_e2e and not args.step_only:
         result["e2e"] = e2e(torch, fcp, w, args, dev, stream, step)
 
-    if not args.step_only:
+    if not args.step_only or args.with_reshuffle:
         result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
     if not args.no_sweep and not args.step_only:
         result["fcp_vs_ring"] = planner_compare(torch, fcp, W, dev, stream, flush, sustained)

@@ -288,27 +288,41 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Row permutation between the user's and the workers' token layouts, 16 bytes per thread
-// per iteration: unit u of a head covers chunk (u % chunks) of worker-layout row
-// (u / chunks); writes (gather) or reads (scatter) of consecutive threads are contiguous.
+// Row permutation between the user's and the workers' token layouts. Thread u of head group
+// blockIdx.y owns 16-byte chunk (u % chunks) of worker-layout row (u / chunks) in eight heads:
+// the row's user index is read once and the eight copies go out together, so each thread
+// keeps eight independent 16-byte loads in flight. Consecutive threads touch consecutive
+// chunks of a row, so the gathered and the scattered side both move whole rows; splitting
+// the heads over the grid's y dimension keeps the CTAs small enough that the SMs finish
+// together.
 template <bool kToWorkers>
 __global__ void __launch_bounds__(256)
     reshuffle_kernel(const int* __restrict__ order, const uint4* __restrict__ src, uint4* __restrict__ dst,
-                     long long T, int chunks, long long total) {
-  const long long per_head = T * chunks;
-  for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
-       u += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long h = u / per_head;
-    const long long r = u - h * per_head;
-    const long long i = r / chunks;
-    const int c = static_cast<int>(r - i * chunks);
-    const long long user = order[i];
-    const long long wi = (h * T + i) * chunks + c;
-    const long long ui = (h * T + user) * chunks + c;
-    if (kToWorkers)
-      dst[wi] = __ldg(src + ui);
-    else
-      dst[ui] = __ldg(src + wi);
+                     long long T, int chunks, int heads) {
+  const long long units = T * chunks;  // (row, chunk) pairs of one head; also the head stride
+  const int groups = (heads + 7) / 8;
+  for (int g = blockIdx.y; g < groups; g += gridDim.y) {
+    const int h0 = g * 8;
+    const int nh = heads - h0 < 8 ? heads - h0 : 8;
+    const uint4* s = src + h0 * units;
+    uint4* d = dst + h0 * units;
+    for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
+         u += static_cast<long long>(gridDim.x) * blockDim.x) {
+      const long long i = u / chunks;
+      const long long c = u - i * chunks;
+      const long long ui = static_cast<long long>(order[i]) * chunks + c;
+      const long long from = kToWorkers ? ui : u;
+      const long long to = kToWorkers ? u : ui;
+      if (nh == 8) {
+        uint4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = __ldg(s + j * units + from);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j * units + to] = x[j];
+      } else {
+        for (int j = 0; j < nh; ++j) d[j * units + to] = __ldg(s + j * units + from);
+      }
+    }
   }
 }
 
@@ -433,19 +447,21 @@ fcp_status fcp_reshuffle(const fcp_plan* plan, const void* d_plan, const void* s
   if (T == 0) return FCP_OK;
   if (!src || !dst || src == dst || !aligned16(src) || !aligned16(dst)) return FCP_ERR_INVALID;
   const int chunks = row_bytes / 16;
-  const long long total = static_cast<long long>(heads) * T * chunks;
+  const long long units = static_cast<long long>(T) * chunks;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long want = (total + 255) / 256;
-  const unsigned grid = static_cast<unsigned>(want < 16LL * sms ? want : 16LL * sms);
+  const long long want = (units + 255) / 256;
+  const int groups = (heads + 7) / 8;
+  const dim3 grid(static_cast<unsigned>(want < 64LL * sms ? want : 64LL * sms),
+                  static_cast<unsigned>(groups < 65535 ? groups : 65535));
   const auto* order = dev_array<int>(d_plan, plan->layout.worker_order);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (direction == 0)
     reshuffle_kernel<true><<<grid, 256, 0, s>>>(order, static_cast<const uint4*>(src), static_cast<uint4*>(dst), T,
-                                               chunks, total);
+                                               chunks, heads);
   else
     reshuffle_kernel<false><<<grid, 256, 0, s>>>(order, static_cast<const uint4*>(src), static_cast<uint4*>(dst), T,
-                                                chunks, total);
+                                                chunks, heads);
   FCP_CUDA_TRY(cudaGetLastError(), "reshuffle launch");
   return FCP_OK;
 }

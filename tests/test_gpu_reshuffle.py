@@ -11,8 +11,12 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("w", [W.tiny_causal(), W.causal_mixed(), W.full_mask()], ids=lambda w: w.name)
-@pytest.mark.parametrize("dtype,width", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 128)])
-def test_reshuffle_matches_oracle_order(fcp, w, dtype, width):
+@pytest.mark.parametrize("dtype,width", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 128),
+                                         (torch.bfloat16, 48)])
+@pytest.mark.parametrize("heads", [3, 19])
+def test_reshuffle_matches_oracle_order(fcp, w, dtype, width, heads):
+    """Heads 3 take only the per-head tail of the copy loop, 19 two groups of eight and a tail;
+    width 48 in bf16 is a 96-byte row, six 16-byte chunks (not a power of two)."""
     part = P.partition(w.seqlens, w.block_size, w.causal)
     dist = P.distribute(part, w.n_workers, w.token_cap)
     order = torch.tensor(P.worker_order(part, dist, w.n_workers), dtype=torch.long)
@@ -20,7 +24,6 @@ def test_reshuffle_matches_oracle_order(fcp, w, dtype, width):
     d_plan = torch.empty(plan.device_bytes(), dtype=torch.uint8, device="cuda")
     plan.upload(d_plan)
     g = torch.Generator(device="cuda").manual_seed(7)
-    heads = 3
     x = torch.randn((heads, w.total_tokens, width), generator=g, device="cuda").to(dtype)
     y = torch.empty_like(x)
     fcp.reshuffle(plan, d_plan, x, y, to_workers=True)
