@@ -255,39 +255,52 @@ def timed_steps(torch, step, steps, warmup, flush, backward=True):
     return out
 
 
-def cpu_baseline_sample(w, target_s=12.0):
-    """The oracle, as it stands, on a bounded sample of the workload: a causal prefix of S
-    tokens of the same sequence with all heads (forward + backward), timed on host cores."""
-    import numpy as np
-    import torch
-
+def oracle_prefix_run(w, S):
+    """One oracle forward + backward on the causal prefix of S tokens of the workload's
+    sequence (all heads), timed on host cores: (seconds, FLOPs)."""
     import workloads as W
     from oracle import attention as A
 
-    def run(S):
-        sub = W.Workload("prefix", [S], w.block_size, w.hq, w.hkv, w.head_dim, 1, w.causal, std=w.std)
-        q, k, v = W.make_qkv(sub)
-        do = W.make_dout(sub)
-        t0 = time.perf_counter()
-        A.attention_forward(q, k, v, sub.seqlens, sub.causal)
-        A.attention_backward(q, k, v, do, sub.seqlens, sub.causal)
-        dt = time.perf_counter() - t0
-        f, b = flops_of(sub.seqlens, sub.causal, sub.hq, sub.head_dim)
-        return dt, f + b
+    sub = W.Workload("prefix", [S], w.block_size, w.hq, w.hkv, w.head_dim, 1, w.causal, std=w.std)
+    q, k, v = W.make_qkv(sub)
+    do = W.make_dout(sub)
+    t0 = time.perf_counter()
+    A.attention_forward(q, k, v, sub.seqlens, sub.causal)
+    A.attention_backward(q, k, v, do, sub.seqlens, sub.causal)
+    dt = time.perf_counter() - t0
+    f, b = flops_of(sub.seqlens, sub.causal, sub.hq, sub.head_dim)
+    return dt, f + b
 
+
+def oracle_prefix_calibrate(w, target_s):
+    """Prefix length whose oracle run takes at least a third of target_s (doubling from 256
+    tokens, at most half the sequence), with that run's (seconds, FLOPs)."""
     S = 256
-    dt, fl = run(S)
+    dt, fl = oracle_prefix_run(w, S)
     while dt < target_s / 3 and S < w.total_tokens // 2:
         S *= 2
-        dt, fl = run(S)
+        dt, fl = oracle_prefix_run(w, S)
+    return S, dt, fl
+
+
+def host_cores():
     try:
-        cores = len(os.sched_getaffinity(0))
+        return len(os.sched_getaffinity(0))
     except AttributeError:
-        cores = os.cpu_count()
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"float64 numpy oracle, forward+backward of the first {S} tokens of the causal sequence, "
-                      f"{w.hq}/{w.hkv} heads, D={w.head_dim} ({dt:.1f} s)",
-            "seconds": dt}
+        return os.cpu_count()
+
+
+def oracle_sample_desc(w, S, dt):
+    return (f"float64 numpy oracle, forward+backward of the first {S} tokens of the causal sequence, "
+            f"{w.hq}/{w.hkv} heads, D={w.head_dim} ({dt:.1f} s)")
+
+
+def cpu_baseline_sample(w, target_s=12.0):
+    """The oracle, as it stands, on a bounded sample of the workload: a causal prefix of S
+    tokens of the same sequence with all heads (forward + backward), timed on host cores."""
+    S, dt, fl = oracle_prefix_calibrate(w, target_s)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+            "sample": oracle_sample_desc(w, S, dt), "seconds": dt}
 
 
 def traffic_from_profile(kernel_tag, block):
@@ -681,26 +694,26 @@ def balance_report(W):
 
 def bench_reference(args):
     """The oracle as it stands, timed on the host cores on bounded samples of the same
-    workload, same metric and unit. Under torchrun only rank 0 runs it."""
+    workload, same metric and unit: the warm-up picks the prefix length (sized so that the
+    K timed steps take about two minutes at most), then exactly K steps are timed at that
+    length. Under torchrun only rank 0 runs it."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = workload(args)
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; kept for the contract's arguments
-    vals = []
-    samples = []
-    for _ in range(max(1, min(args.steps, 3))):
-        c = cpu_baseline_sample(w, target_s=6.0)
-        vals.append(c["value"])
-        samples.append(c)
-    val = statistics.mean(vals)
-    cpu = dict(samples[-1])
-    cpu["value"] = val
-    ms = statistics.mean(c["seconds"] for c in samples) * 1e3
+    per_step = min(6.0, 120.0 / max(1, args.steps))
+    S, _, _ = oracle_prefix_calibrate(w, per_step)  # untimed warm-up and calibration
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_prefix_run(w, S)
+    runs = [oracle_prefix_run(w, S) for _ in range(args.steps)]
+    secs = sum(dt for dt, _ in runs)
+    val = sum(fl for _, fl in runs) / secs / 1e12
+    ms = secs / len(runs) * 1e3
+    cpu = {"value": val, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+           "sample": oracle_sample_desc(w, S, secs / len(runs)), "seconds": secs / len(runs)}
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
-        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": len(vals), "warmup": args.warmup,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": len(runs), "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"causal {w.total_tokens}-token sequence, block {w.block_size}, {w.hq}/{w.hkv} heads, "
