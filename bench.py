@@ -41,7 +41,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step-only", action="store_true",
                     help="only the headline step (for profiling): no e2e, CPU baseline, reshuffle, sweep, "
-                         "planner comparison, solver, pipeline or balance sections")
+                         "configs or merge sections")
+    ap.add_argument("--extras", action="store_true",
+                    help="also report the planner-level sections: FCP against the ring plan through the kernels, "
+                         "the solver's host time, the block-level pipeline by coalesce degree, the balance report")
     ap.add_argument("--with-reshuffle", action="store_true", help="keep the reshuffle section under --step-only")
     ap.add_argument("--block", type=int, default=HEADLINE_BLOCK)
     ap.add_argument("--coalesce", type=int, default=16)
@@ -58,6 +61,17 @@ def workload(args):
     nb = max(1, args.seq_len // args.block)
     return W.Workload(f"causal {args.seq_len}", [args.seq_len], args.block, 64, 8, 128, max(1, nb // 2), True,
                       token_cap=2 * args.block)
+
+
+def config_of(w, coalesce, world):
+    """The workload description both arms print."""
+    return {"workload": f"causal {w.total_tokens}-token sequence, block {w.block_size} "
+                        f"({w.total_tokens // w.block_size} blocks, Zig-Zag LPT over {w.n_workers} workers), "
+                        f"{w.hq}/{w.hkv} heads, D={w.head_dim}, coalesce {coalesce}, fwd+merge+bwd",
+            "block_size": w.block_size, "seq_len": w.total_tokens, "heads_q": w.hq, "heads_kv": w.hkv,
+            "head_dim": w.head_dim, "workers_simulated": w.n_workers, "coalesce": coalesce,
+            "l2": "flushed between steps (512 MB write, untimed); inputs (Q 512 MiB) also exceed L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def peaks():
@@ -180,6 +194,7 @@ class Step:
         per_row_parts = {}
         for r in v["runs"]:
             per_row_parts[(int(r[2]), int(r[3]))] = per_row_parts.get((int(r[2]), int(r[3])), 0) + 1
+        self.parts_per_row = per_row_parts  # (query range) -> partials of each of its rows
         self.merge_bytes = sum(n * qlen * (4 * D + 4) + qlen * (2 * D + 4) for (_, qlen), n in per_row_parts.items()) * hq
         self.n_stages = int(v["n_exec_stages"])
         self.n_launches = 4 + self.n_stages
@@ -360,7 +375,6 @@ def bench_fcp(args):
         times = timed_steps(torch, step, args.steps, args.warmup, flush)
         torch.cuda.synchronize()
         barrier()
-    att = fcp.FcpAttention  # noqa: F841  (public API used below for e2e)
     code = fcp.device_error(step.d_plan, stream)
     if code:
         raise RuntimeError(f"device error word 0x{code:x}")
@@ -379,8 +393,8 @@ def bench_fcp(args):
     dom_flops = step.bwd_flops if dominant == "bwd" else step.fwd_flops
     traffic = traffic_from_profile("bwd_tile_kernel" if dominant == "bwd" else "fwd_kernel", w.block_size) \
         if w.head_dim == 128 and args.seq_len == 32768 else None
-    merge_gbs = step.merge_bytes / (phase["merge"] * 1e-3) / 1e9
 
+    hq, T, D = w.hq, w.total_tokens, w.head_dim
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -395,13 +409,7 @@ def bench_fcp(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"causal {w.total_tokens}-token sequence, block {w.block_size} "
-                               f"({w.total_tokens // w.block_size} blocks, Zig-Zag LPT over {w.n_workers} workers), "
-                               f"{w.hq}/{w.hkv} heads, D={w.head_dim}, coalesce {args.coalesce}, fwd+merge+bwd",
-                   "block_size": w.block_size, "seq_len": w.total_tokens, "heads_q": w.hq, "heads_kv": w.hkv,
-                   "head_dim": w.head_dim, "workers_simulated": w.n_workers, "coalesce": args.coalesce,
-                   "l2": "flushed between steps (512 MB write, untimed); inputs (Q 512 MiB) also exceed L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": config_of(w, args.coalesce, world),
         "fwd_tflops": round(fwd_tf, 2),
         "bwd_tflops": round(bwd_tf, 2),
         "fwd_bwd_frac_of_peak": round(value / world / sustained, 4),
@@ -411,10 +419,6 @@ def bench_fcp(args):
                      "peak": sustained, "unit": "TFLOP/s", "frac": round(dom_tf / sustained, 4),
                      "traffic": traffic, "algorithmic_flops_per_launch": dom_flops,
                      "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a multi-second loop)"},
-        "fwd_roofline": {"bound": "tensor", "achieved": round(fwd_tf, 2), "peak": sustained, "unit": "TFLOP/s",
-                         "frac": round(fwd_tf / sustained, 4)},
-        "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                           "frac": round(merge_gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": step.merge_bytes},
         "gpu_launches": step.n_launches * args.steps,
         "clocks": clk.summary(),
         "imbalance": None,
@@ -426,42 +430,69 @@ def bench_fcp(args):
 
     # end to end through the public API: pinned host inputs -> device, step, results -> host
     if not args.no_e2e and not args.step_only:
-        result["e2e"] = e2e(torch, fcp, w, args, dev, stream, step)
-
-    if not args.step_only or args.with_reshuffle:
-        result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
-    if not args.no_sweep and not args.step_only:
-        result["fcp_vs_ring"] = planner_compare(torch, fcp, W, dev, stream, flush, sustained)
-        result["configs"] = configs_bench(torch, fcp, W, dev, stream, flush, sustained)
-        result["sweep"] = sweep(torch, fcp, W, args, dev, stream, flush, sustained)
-    if rank == 0 and not args.step_only:
-        result["solver"] = solver_report(fcp, W)
-        result["pipeline"] = pipeline_bench(torch, fcp, W, dev, stream, flush, sustained)
-        result["balance"] = balance_report(W)
+        result["e2e"] = e2e(torch, fcp, w, args, dev, stream, step, flush)
     if cpu is not None:
         result["cpu_baseline"] = cpu
+    if args.extras and not args.step_only:
+        result["fcp_vs_ring"] = planner_compare(torch, fcp, W, dev, stream, flush, sustained)
+        if rank == 0:
+            result["solver"] = solver_report(fcp, W)
+            result["pipeline"] = pipeline_bench(torch, fcp, W, dev, stream, flush, sustained)
+            result["balance"] = balance_report(W)
+    # the small sections last, so that the end of the line carries every block size
+    if not args.no_sweep and not args.step_only:
+        result["configs"] = configs_bench(torch, fcp, W, dev, stream, flush, sustained)
+    if not args.step_only or args.with_reshuffle:
+        result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
+    hbm = pk["hbm_gbs"]
+    result["prologue_roofline"] = hbm_roofline(hq * T * (8 * D + 4), phase["prologue"], hbm,
+                                               "prologue_kernel: O, dO in; Di, zeroed dQ acc out")
+    result["convert_roofline"] = hbm_roofline(hq * T * D * 6, phase["convert"], hbm,
+                                              "dq_convert_kernel: f32 dQ in, bf16 dQ out")
+    result["merge_roofline_identity"] = hbm_roofline(
+        step.merge_bytes, phase["merge"], hbm, "merge_kernel in the step: 1 partial per row (copy path), partly in L2")
+    result["fwd_roofline"] = {"kernel": f"fwd_kernel<{D}>", "bound": "tensor", "achieved": round(fwd_tf, 1),
+                              "peak": sustained, "unit": "TFLOP/s", "frac": round(fwd_tf / sustained, 4)}
+    sw = None
+    if not args.no_sweep and not args.step_only:
+        sw, merge_general = sweep(torch, fcp, W, args, dev, stream, flush, sustained, hbm)
+        result["merge_roofline"] = merge_general
+    if sw is not None:
+        result["sweep"] = sw
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def e2e(torch, fcp, w, args, dev, stream, step):
-    """The same metric with host buffers, through the public API (FcpAttention): each step
+def hbm_roofline(nbytes, ms, hbm, what, with_bytes=False):
+    gbs = nbytes / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+    out = {"bound": "hbm", "achieved": round(gbs), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 3)}
+    if with_bytes:
+        out["algorithmic_bytes"] = int(nbytes)
+    out["what"] = what
+    return out
+
+
+def e2e(torch, fcp, w, args, dev, stream, step, flush):
+    """The same metric with host buffers, through the public API (FcpAttention), step for step
+    what the device-timed step does: every step plans the batch again on the host
+    (FcpAttention.replan: partition, distribute, coalesce, device-image upload), flushes L2,
     copies Q, K, V, dO from pinned host memory, runs forward and backward and copies O, LSE,
     dQ, dK, dV back to pinned host memory. The copies run on their own streams, one per
-    direction, into and out of two alternating device buffer sets, so step i+1's inputs
+    direction, into and out of two alternating buffer sets (each with its own FcpAttention,
+    so step i+1's plan upload does not touch the image step i reads), so step i+1's inputs
     arrive and step i's results leave while step i computes; dO travels during step i's
-    forward and O, LSE during its backward. Every step's copies are inside the timed region.
-    `serial` is the same loop with every copy on the compute stream."""
+    forward and O, LSE during its backward. Every step's planning, flush and copies are inside
+    the timed region. `serial` is the same loop with every copy on the compute stream."""
     hq, hkv, T, D = w.hq, w.hkv, w.total_tokens, w.head_dim
     hin = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.do)]
     outs = (step.o, step.lse, step.dq, step.dk, step.dv)
     hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(2)]
     din = [[torch.empty_like(t) for t in (step.q, step.k, step.v, step.do)] for _ in range(2)]
     dout = [[torch.empty_like(t) for t in outs] for _ in range(2)]
-    att = fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, hq, hkv, D, token_cap=w.token_cap,
-                           coalesce=args.coalesce, device=dev)
+    att = [fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, hq, hkv, D, token_cap=w.token_cap,
+                            coalesce=args.coalesce, device=dev) for _ in range(2)]
     h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
     qkv_in, do_in, fwd_done, bwd_done, out_free = ([ev() for _ in range(2)] for _ in range(5))
@@ -472,19 +503,22 @@ def e2e(torch, fcp, w, args, dev, stream, step):
         o, lse, dq, dk, dv = dout[b]
         with torch.cuda.stream(h2d):
             if i >= 2:
-                h2d.wait_event(bwd_done[b])  # set b's inputs were last read by step i-2
+                h2d.wait_event(bwd_done[b])  # set b's plan and inputs were last read by step i-2
+            att[b].replan(stream=h2d)
             for d, h in zip(din[b][:3], hin[:3]):
                 d.copy_(h, non_blocking=True)
             qkv_in[b].record(h2d)
             do.copy_(hin[3], non_blocking=True)
             do_in[b].record(h2d)
+        with torch.cuda.stream(stream):
+            flush.fill_(i & 0xFF)
         stream.wait_event(qkv_in[b])
         if i >= 2:
             stream.wait_event(out_free[b])  # set b's outputs were last read by step i-2's copies
-        att.forward(q, k, v, o=o, lse=lse, stream=stream)
+        att[b].forward(q, k, v, o=o, lse=lse, stream=stream)
         fwd_done[b].record(stream)
         stream.wait_event(do_in[b])
-        att.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, stream=stream)
+        att[b].backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, stream=stream)
         bwd_done[b].record(stream)
         with torch.cuda.stream(d2h):
             d2h.wait_event(fwd_done[b])
@@ -499,10 +533,12 @@ def e2e(torch, fcp, w, args, dev, stream, step):
         q, k, v, do = din[0]
         o, lse, dq, dk, dv = dout[0]
         with torch.cuda.stream(stream):
+            att[0].replan(stream=stream)
+            flush.fill_(i & 0xFF)
             for d, h in zip(din[0], hin):
                 d.copy_(h, non_blocking=True)
-            att.forward(q, k, v, o=o, lse=lse, stream=stream)
-            att.backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, stream=stream)
+            att[0].forward(q, k, v, o=o, lse=lse, stream=stream)
+            att[0].backward(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, stream=stream)
             for h, d in zip(hout[0], (o, lse, dq, dk, dv)):
                 h.copy_(d, non_blocking=True)
 
@@ -525,10 +561,14 @@ def e2e(torch, fcp, w, args, dev, stream, step):
 
     ms = timed(pipelined)
     ms_serial = timed(serial)
+    for a in att:
+        if fcp.device_error(a.d_plan, stream):
+            raise RuntimeError("device error word set in the end-to-end run")
     flops = step.fwd_flops + step.bwd_flops
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
             "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout[0]),
+            "per_step": "plan rebuilt on the host and uploaded, L2 flushed, inputs copied in, results copied out",
             "copies": "h2d and d2h streams, double-buffered: step i+1's inputs and step i's results "
                       "move while step i computes",
             "serial": {"value": round(flops / (ms_serial * 1e-3) / 1e12, 2), "ms_per_step": round(ms_serial, 3)}}
@@ -537,29 +577,57 @@ def e2e(torch, fcp, w, args, dev, stream, step):
 SWEEP_RUNS = 20  # timed runs per sweep point (the median is reported)
 
 
-def sweep(torch, fcp, W, args, dev, stream, flush, sustained):
-    out = []
+def sweep(torch, fcp, W, args, dev, stream, flush, sustained, hbm):
+    """The whole step for every block size (and one partial per pair, c = 1, for b <= 1024):
+    medians over SWEEP_RUNS runs, each with L2 flushed and the plan rebuilt. Compact rows:
+    fwd = forward + merge, bwd = prologue + tiles + dQ conversion, both TFLOP/s. Returns the
+    rows and the merge kernel's roofline on the path that merges (b = 512, c = 1)."""
+    cols = ["block", "coalesce", "fwd_tflops", "bwd_tflops", "fwd_bwd_tflops", "frac_of_peak",
+            "fwd_kernel_tflops", "bwd_kernel_tflops"]
+    rows = []
+    merge_general = None
     for b in SWEEP:
         w = W.block_sweep(b)
         for c in ((args.coalesce, 1) if b <= 1024 else (args.coalesce,)):
             st = Step(fcp, torch, w, c, dev, stream)
             times = timed_steps(torch, st, SWEEP_RUNS, 3, flush)
-            # medians over the runs (each run: L2 flushed, plan rebuilt, whole step)
             fwd = statistics.median(t["fwd"] + t["merge"] for t in times)
             bwd = statistics.median(t["prologue"] + t["bwd"] + t["convert"] for t in times)
             fk = statistics.median(t["fwd"] for t in times)
             bk = statistics.median(t["bwd"] for t in times)
-            ftf = st.fwd_flops / (fwd * 1e-3) / 1e12
-            btf = st.bwd_flops / (bwd * 1e-3) / 1e12
             tot = (st.fwd_flops + st.bwd_flops) / ((fwd + bwd) * 1e-3) / 1e12
-            out.append({"block": b, "blocks": 32768 // b, "coalesce": c, "items": st.plan.view()["n_items"],
-                        "runs_timed": len(times), "statistic": "median",
-                        "fwd_tflops": round(ftf, 1), "bwd_tflops": round(btf, 1), "fwd_bwd_tflops": round(tot, 1),
-                        "fwd_kernel_tflops": round(st.fwd_flops / (fk * 1e-3) / 1e12, 1),
-                        "bwd_kernel_tflops": round(st.bwd_flops / (bk * 1e-3) / 1e12, 1),
-                        "fwd_bwd_frac_of_peak": round(tot / sustained, 4)})
+            rows.append([b, c, round(st.fwd_flops / (fwd * 1e-3) / 1e12), round(st.bwd_flops / (bwd * 1e-3) / 1e12),
+                         round(tot), round(tot / sustained, 3),
+                         round(st.fwd_flops / (fk * 1e-3) / 1e12), round(st.bwd_flops / (bk * 1e-3) / 1e12)])
+            if b == 512 and c == 1:
+                merge_general = merge_cold(torch, fcp, st, stream, flush, hbm)
             del st
             torch.cuda.empty_cache()
+    return {"cols": cols, "rows": rows, "median_of": SWEEP_RUNS}, merge_general
+
+
+def merge_cold(torch, fcp, st, stream, flush, hbm, runs=10):
+    """The LSE merge alone on a plan with many partials per row, L2 flushed before every
+    launch: median GB/s of algorithmic bytes (S partials x (4D+4) read + (2D+4) written per
+    head and token)."""
+    st.run(backward=False)  # the partials of the step's current plan
+    times = []
+    for i in range(runs + 2):
+        with torch.cuda.stream(stream):
+            flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fcp.block_attn_merge(st.plan, st.d_plan, st.part_o, st.part_lse, st.o, st.lse, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    per_row = list(st.parts_per_row.values())
+    out = hbm_roofline(st.merge_bytes, ms, hbm, with_bytes=True, what=
+                       f"merge_kernel alone, {st.w.name} c=1: {min(per_row)}-{max(per_row)} partials per row, "
+                       f"{st.part_o.numel() * 4 / 1e9:.0f} GB of partials, L2 flushed")
+    out["ms"] = round(ms, 3)
     return out
 
 
@@ -579,9 +647,7 @@ def reshuffle_bench(torch, fcp, step, stream, flush, pk):
         if i >= 2:
             times.append(e0.elapsed_time(e1))
     nbytes = 2 * step.q.numel() * step.q.element_size()
-    gbs = nbytes / (statistics.mean(times) * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": nbytes, "kernel": "reshuffle_kernel"}
+    return hbm_roofline(nbytes, statistics.mean(times), pk["hbm_gbs"], "reshuffle_kernel: Q, user to worker layout")
 
 
 def planner_compare(torch, fcp, W, dev, stream, flush, sustained):
@@ -637,28 +703,30 @@ def configs_bench(torch, fcp, W, dev, stream, flush, sustained):
     """The other named workloads, through the same step: the full-mask batch (16 lognormal
     sequences, 65536 tokens, 1K blocks, 8 workers; forward + merge only), the causal mixed
     batch (lognormal lengths plus a 32K outlier, 4K blocks, 16 workers) and the 524288-token
-    causal sequence (8K blocks, 32 workers; 1 warm-up and 1 timed step: about 12 s each).
-    Coalesce degree 16; L2 flushed between steps; medians of the timed steps."""
-    out = []
-    for w, steps, warm in ((W.full_mask(), 5, 2), (W.causal_mixed(), 5, 2), (W.long_causal(), 1, 1)):
+    causal sequence (8K blocks, 32 workers; 1 warm-up and 2 timed steps of about 12 s each).
+    Coalesce degree 16; L2 flushed between steps; medians of the timed steps. Compact rows:
+    TFLOP/s of fwd (+ merge), bwd (prologue + tiles + conversion) and the step, then the
+    per-phase milliseconds."""
+    cols = ["workload", "tokens", "block", "fwd_tflops", "bwd_tflops", "fwd_bwd_tflops", "frac_of_peak",
+            "ms_fwd_kernel", "ms_merge", "ms_prologue", "ms_bwd_kernel", "ms_convert"]
+    rows = []
+    for w, steps, warm in ((W.full_mask(), 5, 2), (W.causal_mixed(), 5, 2), (W.long_causal(), 2, 1)):
         st = Step(fcp, torch, w, 16, dev, stream)
         times = timed_steps(torch, st, steps, warm, flush, backward=w.backward)
+        med = {k: statistics.median(t[k] for t in times) for k in ("fwd", "merge", "prologue", "bwd", "convert")}
         fwd = statistics.median(t["fwd"] + t["merge"] for t in times)
-        row = {"workload": w.name, "tokens": w.total_tokens, "block": w.block_size, "workers": w.n_workers,
-               "causal": w.causal, "fwd_ms": round(fwd, 3),
-               "fwd_tflops": round(st.fwd_flops / (fwd * 1e-3) / 1e12, 1)}
+        ftf = st.fwd_flops / (fwd * 1e-3) / 1e12
+        btf = tot = None
         if w.backward:
             bwd = statistics.median(t["prologue"] + t["bwd"] + t["convert"] for t in times)
-            tot = statistics.median(t["total"] for t in times)
-            row.update({"bwd_ms": round(bwd, 3), "bwd_tflops": round(st.bwd_flops / (bwd * 1e-3) / 1e12, 1),
-                        "fwd_bwd_tflops": round((st.fwd_flops + st.bwd_flops) / (tot * 1e-3) / 1e12, 1)})
-            row["frac_of_peak"] = round(row["fwd_bwd_tflops"] / sustained, 4)
-        else:
-            row["frac_of_peak"] = round(row["fwd_tflops"] / sustained, 4)
-        out.append(row)
+            btf = round(st.bwd_flops / (bwd * 1e-3) / 1e12)
+            tot = round((st.fwd_flops + st.bwd_flops) / (statistics.median(t["total"] for t in times) * 1e-3) / 1e12)
+        rows.append([w.name, w.total_tokens, w.block_size, round(ftf), btf, tot,
+                     round((tot if tot is not None else ftf) / sustained, 3)] +
+                    [round(med[k], 2) for k in ("fwd", "merge", "prologue", "bwd", "convert")])
         del st
         torch.cuda.empty_cache()
-    return out
+    return {"cols": cols, "rows": rows}
 
 
 def solver_report(fcp, W):
@@ -716,8 +784,7 @@ def bench_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": len(runs), "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"causal {w.total_tokens}-token sequence, block {w.block_size}, {w.hq}/{w.hkv} heads, "
-                               f"D={w.head_dim}; oracle on a bounded causal prefix per step"},
+        "config": config_of(w, args.coalesce, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": cpu,
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)

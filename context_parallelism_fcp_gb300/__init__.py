@@ -460,18 +460,43 @@ class FcpAttention:
     def __init__(self, seqlens: Sequence[int], block_size: int, causal: bool, n_workers: int, hq: int, hkv: int,
                  head_dim: int, token_cap: Optional[int] = None, coalesce: int = 1, device="cuda",
                  backward: bool = True, pipeline: Optional[int] = None):
+        self._recipe = (int(block_size), bool(causal), int(n_workers), token_cap, int(coalesce), pipeline)
+        self._setup(self._make_plan(seqlens), hq, hkv, head_dim, device, backward)
+
+    def _make_plan(self, seqlens) -> "Plan":
+        block_size, causal, n_workers, token_cap, coalesce, pipeline = self._recipe
         plan = Plan(seqlens, block_size, causal).distribute(n_workers, token_cap)
         if pipeline is not None:
             plan.schedule(pipeline)
         elif coalesce != 1:
             plan.coalesce(coalesce)
-        self._setup(plan, hq, hkv, head_dim, device, backward)
+        return plan
+
+    def replan(self, seqlens: Optional[Sequence[int]] = None, stream=None) -> None:
+        """Plan a new batch (by default the same lengths again) with the same block size,
+        mask, workers, cap and coalescing, as a training loop does for every batch: partition,
+        distribute and coalesce run on the host, and the new device image is uploaded in
+        ``stream`` order, so kernels enqueued earlier on that stream still see the old plan.
+        The batch must fit the buffers allocated at construction (same total tokens, no more
+        partial rows or device-image bytes)."""
+        if getattr(self, "_recipe", None) is None:
+            raise RuntimeError("replan needs an FcpAttention built from a batch description, not from_plan")
+        plan = self._make_plan(self.plan.seqlens if seqlens is None else seqlens)
+        v = plan.view()
+        if (int(v["total_tokens"]) != self.T or int(v["partial_rows"]) > self.part_o.shape[1]
+                or plan.device_bytes() > self.d_plan.numel()):
+            raise ValueError("the new batch does not fit the buffers of this FcpAttention")
+        if int(v["n_exec_stages"]) != self.n_stages:
+            raise ValueError("the new batch has a different number of pipeline stages")
+        plan.upload(self.d_plan, stream)
+        self.plan = plan
 
     @classmethod
     def from_plan(cls, plan: "Plan", hq: int, hkv: int, head_dim: int, device="cuda",
                   backward: bool = True) -> "FcpAttention":
         """Wrap an already distributed plan (e.g. Plan.ring(...))."""
         self = cls.__new__(cls)
+        self._recipe = None
         self._setup(plan, hq, hkv, head_dim, device, backward)
         return self
 
