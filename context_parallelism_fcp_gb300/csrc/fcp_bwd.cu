@@ -116,7 +116,8 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_bwd_scratch on the current device. The host-side name of the array
 // is only a stand-in, so the address is looked up once per device (with that device
-// current) and cached.
+// current) and cached for the life of the process; a cudaDeviceReset discards the array
+// with the context, so the entry point is not for use on a device after a reset.
 fcp_status static_scratch(void** out) {
   int dev = 0;
   FCP_CUDA_TRY(cudaGetDevice(&dev), "static scratch: current device");

@@ -79,9 +79,10 @@ enum : int {
   B_ACCDONE = B_DQEMPTY + 2,
   B_STGFULL = B_ACCDONE + 1,       // the dQ staging tile is written
   B_STGFREE = B_STGFULL + 1,       // the previous reduce has read the staging tile
-  B_COUNT = B_STGFREE + 1
+  B_DRAIN = B_STGFREE + 1,         // every MMA the CTA issued has completed
+  B_COUNT = B_DRAIN + 1
 };
-static_assert(B_COUNT * 8 + 8 <= 256, "barrier area");
+static_assert(B_COUNT * 8 + 12 <= 256, "barrier area");
 
 // S^T, dP^T: M = 128 keys, N = 64 queries, both operands K-major.
 constexpr uint32_t kIdescST = idesc_bf16(kBN, kBQ, false, false);
@@ -121,6 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + B_COUNT * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + B_COUNT * 8 + 4);
+  // set when an aborted CTA could not confirm that its issued copies or MMAs have finished
+  volatile int* unquiesced = reinterpret_cast<volatile int*>(smem + kOffBar + B_COUNT * 8 + 8);
   float* vec = reinterpret_cast<float*>(smem + kOffVec);  // [stage][lse2[64] | di[64]]
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8 * i; };
 
@@ -150,7 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_ACCDONE), 1);
     mbar_init(bar(B_STGFULL), C::kDrainWarps);
     mbar_init(bar(B_STGFREE), 1);
+    mbar_init(bar(B_DRAIN), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
+    *unquiesced = 0;
     mbar_fence_init();
   }
   if (warp == 13) {
@@ -190,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 12) {
     // ---------------------------------------------------------------- producer
     bool ok = !skip;
+    int last_step[kStages];  // last step whose Q/dO loads went out on each stage
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) last_step[st] = -1;
     if (ok && lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -219,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sb + kOffDO + s * kQTile + p * kQPanel, &tmDO, bar(B_QFULL + s), p * 64, qrow0, h);
           }
         }
+        last_step[s] = step;
         // LSE in log2 units and Di of the step's query rows; rows past the range get
         // LSE = +inf (P = 0) and Di = 0
         float* v = vec + s * 2 * kBQ;
@@ -233,6 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_warp(bar(B_QFULL + s));
         return true;
       });
+    }
+    if (!skip && *abort_flag && lane == 0) {
+      // the loads already issued land in this CTA's shared memory: wait for them (bounded)
+      bool done = mbar_wait_quiesce(bar(B_KVFULL), 0, kWaitLimitNs);
+      for (int st = 0; st < kStages; ++st)
+        if (last_step[st] >= 0)
+          done = mbar_wait_quiesce(bar(B_QFULL + st), (last_step[st] / kStages) & 1, kWaitLimitNs) && done;
+      if (!done) *unquiesced = 1;
     }
   } else if (warp == 13) {
     // ---------------------------------------------------------------- MMA issuer
@@ -303,7 +320,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit_w(bar(B_QEMPTY + s));
       }
       n_steps = total;
-      tc_commit_w(bar(B_ACCDONE));
+      if (ok) tc_commit_w(bar(B_ACCDONE));
+      // every issued MMA has completed once the drain barrier fires; wait for it also after
+      // an abort (the wait ignores the abort flag) so that none still reads shared memory or
+      // writes tensor memory when they are released
+      tc_commit_w(bar(B_DRAIN));
+      if (!__all_sync(0xffffffffu, mbar_wait_quiesce(bar(B_DRAIN), 0, kWaitLimitNs)) && lane == 0) {
+        *abort_flag = 1;
+        *unquiesced = 1;
+        atomicCAS(a.err, 0, kErrBwdWait + 14);
+      }
     }
   } else if (warp < 8) {
     // ---------------------------------------------------------------- gradient warps
@@ -468,12 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (*abort_flag) {
+  tc_fence_before();
+  __syncthreads();
+  if (*unquiesced) {
+    // fallback only: an issued copy or MMA did not report completion within the wait limit
     const unsigned long long t0 = globaltimer();
     while (globaltimer() - t0 < 1000000ull) __nanosleep(1000);
   }
-  tc_fence_before();
-  __syncthreads();
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

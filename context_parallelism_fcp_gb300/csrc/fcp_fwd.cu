@@ -70,7 +70,7 @@ enum : int {
 // barrier area: mbarriers, abort flag, TMEM base, then the 2-slot tile ring (48 bytes a slot)
 constexpr int kTileSlotOff = 256;
 constexpr int kBarArea = kTileSlotOff + 2 * 48;
-static_assert(B_COUNT * 8 + 8 <= kTileSlotOff, "barrier area");
+static_assert(B_COUNT * 8 + 12 <= kTileSlotOff, "barrier area");
 
 template <int D>
 struct FwdCfg {
@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t sb = smem_u32(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kBar + B_COUNT * 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBar + B_COUNT * 8 + 4);
+  // set when an aborted CTA could not confirm that its issued copies or MMAs have finished
+  volatile int* unquiesced = reinterpret_cast<volatile int*>(smem + C::kBar + B_COUNT * 8 + 8);
   auto bar = [&](int i) -> uint32_t { return sb + C::kBar + 8 * i; };
 
   const int warp = threadIdx.x >> 5;
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(B_TEMPTY + k), 9);
     }
     *abort_flag = (*reinterpret_cast<volatile int*>(a.err) != 0) ? 1 : 0;
+    *unquiesced = 0;
     mbar_fence_init();
   }
   if (warp == 9) {
@@ -207,6 +210,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tmV);
       int J = 0;
       bool ok = true;
+      int last_q = -1, last_k[2] = {-1, -1}, last_v[2] = {-1, -1};  // last issued load per barrier
       for (int u = 0; ok; ++u) {
         const int k = u & 1;
         if (!mbar_wait(bar(B_TEMPTY + k), ((u >> 1) & 1) ^ 1, abort_flag, a.err, kErrFwdWait + 13)) break;
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_3d(sb + C::kQ0 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, T.h0);
           tma_load_3d(sb + C::kQ1 + p * kPanelBytes, &tmQ, bar(B_QFULL), p * 64, qrow, T.h1);
         }
+        last_q = u;
         for (int ii = T.item_begin; ii < T.item_end && ok; ++ii) {
           const fcp_item itm = a.items[ii];
           const int nkt = kv_tiles(itm, T.qt);
@@ -251,14 +256,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int p = 0; p < C::kPanels; ++p)
               tma_load_3d(sb + C::kK + s * C::kTileBytes + p * kPanelBytes, &tmK, bar(B_KFULL + s), p * 64, kvrow,
                           T.kvh);
+            last_k[s] = J;
             if (!mbar_wait(bar(B_VEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 2)) { ok = false; break; }
             mbar_arrive_expect_tx(bar(B_VFULL + s), C::kTileBytes);
 #pragma unroll
             for (int p = 0; p < C::kPanels; ++p)
               tma_load_3d(sb + C::kV + s * C::kTileBytes + p * kPanelBytes, &tmV, bar(B_VFULL + s), p * 64, kvrow,
                           T.kvh);
+            last_v[s] = J;
           }
         }
+      }
+      if (*abort_flag) {
+        // the loads already issued land in this CTA's shared memory: wait for them (bounded)
+        bool done = last_q < 0 || mbar_wait_quiesce(bar(B_QFULL), last_q & 1, kWaitLimitNs);
+        for (int st = 0; st < 2; ++st) {
+          if (last_k[st] >= 0) done = mbar_wait_quiesce(bar(B_KFULL + st), (last_k[st] >> 1) & 1, kWaitLimitNs) && done;
+          if (last_v[st] >= 0) done = mbar_wait_quiesce(bar(B_VFULL + st), (last_v[st] >> 1) & 1, kWaitLimitNs) && done;
+        }
+        if (!done) *unquiesced = 1;
       }
     }
   } else if (warp == 9) {
@@ -349,9 +365,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_commit_w(bar(B_QEMPTY));
         if (jl > 0) ok = finish_pv(J, jl, u, true);
       }
-      // every issued MMA has completed once the drain barrier fires
+      // every issued MMA has completed once the drain barrier fires; wait for it also after
+      // an abort (the wait ignores the abort flag), so that no MMA still reads shared memory
+      // or writes tensor memory when they are released
       tc_commit_w(bar(B_DRAIN));
-      wwait(bar(B_DRAIN), 0, kErrFwdWait + 7);
+      if (!__all_sync(0xffffffffu, mbar_wait_quiesce(bar(B_DRAIN), 0, kWaitLimitNs)) && lane == 0) {
+        *abort_flag = 1;
+        *unquiesced = 1;
+        atomicCAS(a.err, 0, kErrFwdWait + 7);
+      }
     }
   } else if (!skip) {
     // ------------------------------------------------------------ softmax (warps 0-7)
@@ -511,13 +533,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   }
 
-  if (*abort_flag) {
-    // let in-flight asynchronous copies land before the CTA's shared memory is released
+  tc_fence_before();
+  __syncthreads();
+  if (*unquiesced) {
+    // fallback only: an issued copy or MMA did not report completion within the wait limit
     const unsigned long long t0 = globaltimer();
     while (globaltimer() - t0 < 1000000ull) __nanosleep(1000);
   }
-  tc_fence_before();
-  __syncthreads();
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

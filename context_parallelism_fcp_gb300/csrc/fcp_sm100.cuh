@@ -86,6 +86,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Wait for a phase regardless of the CTA's abort flag, for at most limit_ns. Used on the way
+// out of an aborted CTA so that copies and MMAs it has already issued finish before its
+// shared and tensor memory are released. Returns false if the phase did not complete in time.
+__device__ __forceinline__ bool mbar_wait_quiesce(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 // 3-D tiled tensor load into shared memory, completing `bytes` on the mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,

@@ -292,8 +292,10 @@ fcp_status fcp_block_attn_bwd_dq_convert(const fcp_plan* plan, const float* dq_a
  * of fcp_bwd_static_scratch_bytes() = 32 MiB inside the library, which every GPU that loads
  * the library holds until the process exits. A larger requirement returns
  * FCP_ERR_UNSUPPORTED with the sizes in fcp_last_error(). The first call on a device looks
- * up the array's device address with that device current; make that first call before any
- * stream capture. All calls share the one array: calls whose work overlaps on the GPU (other
+ * up the array's device address with that device current and keeps it for the life of the
+ * process; make that first call before any stream capture, and do not use this entry point
+ * on a device after cudaDeviceReset (the reset discards the array, and the kept address
+ * would be stale). All calls share the one array: calls whose work overlaps on the GPU (other
  * streams, other threads) race on it and must be serialised by the caller. Each call
  * re-zeroes the accumulator itself, so nothing needs clearing between calls. */
 size_t fcp_bwd_static_scratch_bytes(void);

@@ -2,12 +2,14 @@
 and compare against the float64 oracle, in full or on sampled rows.
 
 Tolerances. Forward (fixed by the target): O max-abs <= 2e-2 and mean-abs <= 2e-3 against
-the oracle, LSE max-abs <= 1e-3. Backward (derived from bf16 arithmetic): the kernels round
-P and dS to bf16 (unit roundoff u = 2^-8) before the gradient MMAs and the outputs to bf16,
-so each gradient element carries a relative error of a few u; the tests require
-max-abs <= 5e-2 * max(1, max|ref|) and mean-abs <= 1e-2 * mean|ref| + 1e-5 (about 2.5 u,
-with an absolute floor for gradients that cancel to exactly zero, e.g. dQ of a one-token
-sequence, where the kernel returns rounding noise of order u * |dP|) per tensor.
+the oracle, LSE max-abs <= 1e-3. Backward (derived from bf16 arithmetic): the outputs are
+bf16, whose rounding alone leaves a mean relative error of about 0.7 * 2^-9 = 1.4e-3 (the
+error is uniform on +-ulp/2 and ulp/|x| runs over (2^-8, 2^-7]); the kernels also round P and dS to
+bf16 before the gradient MMAs and form Di from the bf16 O. The tests require, per tensor,
+max-abs <= 2e-2 * max(1, max|ref|) and mean-abs <= 5e-3 * mean|ref| + 1e-5 (the absolute
+floor covers gradients that cancel to exactly zero, e.g. dQ of a one-token sequence, where
+the kernel returns rounding noise of order u * |dP|). Every comparison is recorded, so a run
+reports how much of each bound it used (tests/conftest.py prints the largest share).
 """
 from __future__ import annotations
 
@@ -20,7 +22,7 @@ import workloads as W
 from oracle import attention as A
 
 O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
-G_MAX_REL, G_MEAN_REL, G_MEAN_ABS = 5e-2, 1e-2, 1e-5
+G_MAX_REL, G_MEAN_REL, G_MEAN_ABS = 2e-2, 5e-3, 1e-5
 
 # Every comparison appends (test, where, tensor, max err, max bound, mean err, mean bound),
 # so that a run can report how much of each bound the observed errors use.

@@ -54,8 +54,9 @@ def test_static_scratch_rejects_oversize(fcp):
     w = W.causal_mixed()  # 64 heads x 65536 tokens x 129 floats: far beyond the array
     plan = fcp.Plan(w.seqlens, w.block_size, w.causal).distribute(w.n_workers)
     assert plan.workspace_bytes(w.hq, w.head_dim) > L.fcp_bwd_static_scratch_bytes()
-    d = ctypes.c_void_p(256)
-    st = L.fcp_block_attn_bwd_static_scratch(plan.handle, d, d, d, d, d, d, d, w.hq, w.hkv, w.head_dim, d, d, d,
-                                             None)
+    # null device pointers: the size check comes first, and if it ever did not, the call would
+    # stop at the pointer checks instead of launching anything
+    st = L.fcp_block_attn_bwd_static_scratch(plan.handle, None, None, None, None, None, None, None, w.hq, w.hkv,
+                                             w.head_dim, None, None, None, None)
     assert st == 3
     assert b"exceeds" in L.fcp_last_error()
