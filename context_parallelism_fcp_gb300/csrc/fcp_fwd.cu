@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tmV);
       int J = 0;
       bool ok = true;
-      int last_q = -1, last_k[2] = {-1, -1}, last_v[2] = {-1, -1};  // last issued load per barrier
+      int last_q = -1, last_kj = -1, last_vj = -1;  // tile of the last Q load, key tile of the last K, V loads
       for (int u = 0; ok; ++u) {
         const int k = u & 1;
         if (!mbar_wait(bar(B_TEMPTY + k), ((u >> 1) & 1) ^ 1, abort_flag, a.err, kErrFwdWait + 13)) break;
@@ -256,24 +256,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int p = 0; p < C::kPanels; ++p)
               tma_load_3d(sb + C::kK + s * C::kTileBytes + p * kPanelBytes, &tmK, bar(B_KFULL + s), p * 64, kvrow,
                           T.kvh);
-            last_k[s] = J;
+            last_kj = J;
             if (!mbar_wait(bar(B_VEMPTY + s), ph ^ 1, abort_flag, a.err, kErrFwdWait + 2)) { ok = false; break; }
             mbar_arrive_expect_tx(bar(B_VFULL + s), C::kTileBytes);
 #pragma unroll
             for (int p = 0; p < C::kPanels; ++p)
               tma_load_3d(sb + C::kV + s * C::kTileBytes + p * kPanelBytes, &tmV, bar(B_VFULL + s), p * 64, kvrow,
                           T.kvh);
-            last_v[s] = J;
+            last_vj = J;
           }
         }
       }
       if (*abort_flag) {
         // the loads already issued land in this CTA's shared memory: wait for them (bounded)
+        // (a K/V stage is reused only after its previous tile was consumed, so only the last
+        // two key tiles can still be in flight)
         bool done = last_q < 0 || mbar_wait_quiesce(bar(B_QFULL), last_q & 1, kWaitLimitNs);
-        for (int st = 0; st < 2; ++st) {
-          if (last_k[st] >= 0) done = mbar_wait_quiesce(bar(B_KFULL + st), (last_k[st] >> 1) & 1, kWaitLimitNs) && done;
-          if (last_v[st] >= 0) done = mbar_wait_quiesce(bar(B_VFULL + st), (last_v[st] >> 1) & 1, kWaitLimitNs) && done;
-        }
+        for (int j = last_kj > 0 ? last_kj - 1 : 0; j <= last_kj; ++j)
+          done = mbar_wait_quiesce(bar(B_KFULL + (j & 1)), (j >> 1) & 1, kWaitLimitNs) && done;
+        for (int j = last_vj > 0 ? last_vj - 1 : 0; j <= last_vj; ++j)
+          done = mbar_wait_quiesce(bar(B_VFULL + (j & 1)), (j >> 1) & 1, kWaitLimitNs) && done;
         if (!done) *unquiesced = 1;
       }
     }

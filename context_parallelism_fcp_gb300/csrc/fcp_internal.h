@@ -68,7 +68,7 @@ enum DevError : int32_t {
   kErrSmemAlign = 0x01,
   kErrFwdWait = 0x10,
   kErrBwdWait = 0x20,
-  kErrSelfTest = 0x40,  // the bounded-wait self-test gave up, as it must
+  kErrSelfTest = 0x40,  // the bounded-wait self-test gave up, as it must (0x41: its second wait)
 };
 
 void set_last_error(const std::string& msg);

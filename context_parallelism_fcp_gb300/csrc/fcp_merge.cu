@@ -362,18 +362,24 @@ using namespace fcp;
 namespace fcp {
 namespace {
 
-// One thread waits, with the kernels' bounded mbarrier wait, on a barrier that nothing ever
-// completes; after the wait's limit it raises the abort flag and records kErrSelfTest.
+// Two threads wait on barriers that nothing ever completes, each with one of the kernels'
+// bounded waits: thread 0 with the polling wait of the forward (it records kErrSelfTest in
+// the error word), thread 32 with the poll-then-suspend wait of the backward (it records
+// kErrSelfTest + 1 in the word after it). Each gives up after the wait limit and returns.
 __global__ void bounded_wait_selftest_kernel(int* err) {
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int abort_flag;
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int abort_flag[2];
   if (threadIdx.x == 0) {
-    dev::mbar_init(dev::smem_u32(&bar), 1);
-    abort_flag = 0;
+    dev::mbar_init(dev::smem_u32(&bar[0]), 1);
+    dev::mbar_init(dev::smem_u32(&bar[1]), 1);
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
     dev::mbar_fence_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) dev::mbar_wait(dev::smem_u32(&bar), 0, &abort_flag, err, kErrSelfTest);
+  if (threadIdx.x == 0) dev::mbar_wait(dev::smem_u32(&bar[0]), 0, &abort_flag[0], err, kErrSelfTest);
+  if (threadIdx.x == 32)
+    dev::mbar_wait_backoff<64, 1000u>(dev::smem_u32(&bar[1]), 0, &abort_flag[1], err + 1, kErrSelfTest + 1);
 }
 
 }  // namespace
@@ -394,7 +400,7 @@ fcp_status fcp_plan_upload(const fcp_plan* plan, void* d_plan, size_t bytes, voi
 fcp_status fcp_selftest_bounded_wait(void* d_plan, void* stream) {
   if (d_plan == nullptr || (reinterpret_cast<uintptr_t>(d_plan) & 255u) != 0) return FCP_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  fcp::bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(fcp::dev_error_word(d_plan));
+  fcp::bounded_wait_selftest_kernel<<<1, 64, 0, s>>>(fcp::dev_error_word(d_plan));
   FCP_CUDA_TRY(cudaGetLastError(), "bounded-wait self-test launch");
   return FCP_OK;
 }

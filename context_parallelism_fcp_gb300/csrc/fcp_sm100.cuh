@@ -97,6 +97,47 @@ __device__ __forceinline__ bool mbar_wait_quiesce(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// try_wait with a suspend-time hint: if the phase is not complete the thread may sleep for up
+// to hint_ns (or until the phase completes) instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for kernels whose waiting warps share the SM with long-running work: after kSpin
+// plain polls the thread suspends between polls (up to kHintNs each), so that waits of
+// hundreds of cycles stop spending issue slots and power. Same contract as mbar_wait.
+template <int kSpin, uint32_t kHintNs>
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                                  int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+#pragma unroll 1
+  for (int i = 0; i < kSpin; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_suspend(bar, parity, kHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, code);
+      __threadfence();
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 // 3-D tiled tensor load into shared memory, completing `bytes` on the mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,

@@ -320,12 +320,14 @@ fcp_status fcp_reshuffle(const fcp_plan* plan, const void* d_plan, const void* s
  * kernel and wait that gave up) and clear it. Returns FCP_ERR_DEVICE if it was set. */
 fcp_status fcp_device_error(const void* d_plan, int32_t* code, void* stream);
 
-/* Self-test of the device-side failure path (no counterpart on the pages): one thread waits,
- * with the bounded mbarrier wait every tile kernel uses, on a barrier that nothing ever
- * completes. After the wait's 2-second limit it records code 0x40 in the error word of
- * d_plan (a device buffer of at least 256 bytes, 256-byte aligned, whose error word should
- * be clear) and the kernel exits; the context stays usable. Read the result with
- * fcp_device_error. Errors: FCP_ERR_INVALID, FCP_ERR_CUDA. */
+/* Self-test of the device-side failure path (no counterpart on the pages): two threads wait,
+ * each with one of the bounded mbarrier waits the tile kernels use (the polling wait of the
+ * forward, the poll-then-suspend wait of the backward), on barriers that nothing ever
+ * completes. After the waits' 2-second limit the first records code 0x40 in the error word of
+ * d_plan (int32 word 0) and the second code 0x41 in int32 word 1, and the kernel exits; the
+ * context stays usable. d_plan is a device buffer of at least 256 bytes, 256-byte aligned,
+ * whose first two words should be clear. Read word 0 with fcp_device_error. Errors:
+ * FCP_ERR_INVALID, FCP_ERR_CUDA. */
 fcp_status fcp_selftest_bounded_wait(void* d_plan, void* stream);
 
 void fcp_plan_free(fcp_plan* plan);
