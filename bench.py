@@ -428,6 +428,12 @@ def bench_fcp(args):
     mx = max(loads)
     result["imbalance"] = round((mx - sum(loads) / len(loads)) / mx, 6) if mx else 0.0
 
+    resh = None
+    if not args.step_only or args.with_reshuffle:
+        # measured here, right after the headline step: after the 524288-token workload of
+        # `configs` the same launches ran about 20% slower
+        resh = reshuffle_bench(torch, fcp, step, stream, flush, pk)
+
     # end to end through the public API: pinned host inputs -> device, step, results -> host
     if not args.no_e2e and not args.step_only:
         result["e2e"] = e2e(torch, fcp, w, args, dev, stream, step, flush)
@@ -442,8 +448,8 @@ def bench_fcp(args):
     # the small sections last, so that the end of the line carries every block size
     if not args.no_sweep and not args.step_only:
         result["configs"] = configs_bench(torch, fcp, W, dev, stream, flush, sustained)
-    if not args.step_only or args.with_reshuffle:
-        result["reshuffle_roofline"] = reshuffle_bench(torch, fcp, step, stream, flush, pk)
+    if resh is not None:
+        result["reshuffle_roofline"] = resh
     hbm = pk["hbm_gbs"]
     result["prologue_roofline"] = hbm_roofline(hq * T * (8 * D + 4), phase["prologue"], hbm,
                                                "prologue_kernel: O, dO in; Di, zeroed dQ acc out")
