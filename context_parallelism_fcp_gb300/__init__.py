@@ -509,7 +509,9 @@ class FcpAttention:
         self.T = sum(int(x) for x in plan.seqlens)
         self.device = torch.device(device)
         nbytes = self.plan.device_bytes()
-        self.d_plan = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        # room for the device images of later batches of the same size (replan), whose
+        # work lists differ in length
+        self.d_plan = torch.empty(max(2 * nbytes, 65536), dtype=torch.uint8, device=self.device)
         self.plan.upload(self.d_plan)
         ob, lb = self.plan.partial_sizes(hq, head_dim)
         rows = self.plan.view()["partial_rows"]
