@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--with-reshuffle", action="store_true", help="keep the reshuffle section under --step-only")
     ap.add_argument("--block", type=int, default=HEADLINE_BLOCK)
     ap.add_argument("--coalesce", type=int, default=16)
+    ap.add_argument("--bwd-band", type=int, default=None,
+                    help="rows per backward query band (0: none; default: the plan's choice)")
     ap.add_argument("--seq-len", type=int, default=32768,
                     help="length of the causal sequence (smaller values are for profiler captures)")
     return ap.parse_args()
@@ -163,9 +165,11 @@ class ClockSampler:
 class Step:
     """Buffers and launches of one batch; run() enqueues one whole step on `stream`."""
 
-    def __init__(self, fcp, torch, w, coalesce, device, stream, planner="fcp", pipeline=None, replan=True):
+    def __init__(self, fcp, torch, w, coalesce, device, stream, planner="fcp", pipeline=None, replan=True,
+                 bwd_band=None):
         import workloads as W
 
+        self.bwd_band = bwd_band
         self.fcp, self.torch, self.w, self.c, self.dev, self.stream = fcp, torch, w, coalesce, device, stream
         self.planner = planner
         self.pipeline = pipeline  # coalesce degree of the block-level pipeline, or None
@@ -186,6 +190,10 @@ class Step:
         self.dv = torch.empty_like(self.v)
         self.dq_acc = torch.empty((hq, T, D), dtype=torch.float32, device=device)
         self.di = torch.empty((hq, T), dtype=torch.float32, device=device)
+        # the backward runs in query bands when the plan has them (long batches)
+        self.n_bands = plan.bwd_bands()[0]
+        self.dkv_acc = (torch.empty(plan.band_workspace_bytes(hkv, D), dtype=torch.uint8, device=device)
+                        if self.n_bands else None)
         self.plan = plan
         self.fwd_flops, self.bwd_flops = flops_of(w.seqlens, w.causal, hq, D)
         self.events = None
@@ -197,7 +205,9 @@ class Step:
         self.parts_per_row = per_row_parts  # (query range) -> partials of each of its rows
         self.merge_bytes = sum(n * qlen * (4 * D + 4) + qlen * (2 * D + 4) for (_, qlen), n in per_row_parts.items()) * hq
         self.n_stages = int(v["n_exec_stages"])
-        self.n_launches = 4 + self.n_stages
+        # forward stages, merge, prologue, backward tiles (one per query band, then the dK and dV
+        # conversions), dQ conversion
+        self.n_launches = self.n_stages + 2 + (self.n_bands + 2 if self.n_bands else 1) + 1
         if not replan:
             plan.upload(self.d_plan, stream)
 
@@ -206,7 +216,10 @@ class Step:
         if self.planner == "ring":
             plan = self.fcp.Plan.ring(w.seqlens, w.n_workers, w.causal)
         else:
-            plan = self.fcp.Plan(w.seqlens, w.block_size, w.causal).distribute(w.n_workers, w.token_cap)
+            plan = self.fcp.Plan(w.seqlens, w.block_size, w.causal)
+            if self.bwd_band is not None:
+                plan.set_bwd_band(self.bwd_band)
+            plan.distribute(w.n_workers, w.token_cap)
         if self.pipeline is not None:
             plan.schedule(self.pipeline)
         elif self.c != 1:
@@ -237,8 +250,12 @@ class Step:
         if backward:
             f.block_attn_bwd_prologue(plan, self.o, self.do, self.di, self.dq_acc, s)
             rec(3)
-            f.block_attn_bwd_tiles(plan, self.d_plan, self.q, self.k, self.v, self.do, self.lse, self.di,
-                                   self.dq_acc, self.dk, self.dv, s)
+            if self.n_bands:
+                f.block_attn_bwd_tiles_banded(plan, self.d_plan, self.q, self.k, self.v, self.do, self.lse, self.di,
+                                              self.dq_acc, self.dkv_acc, self.dk, self.dv, s)
+            else:
+                f.block_attn_bwd_tiles(plan, self.d_plan, self.q, self.k, self.v, self.do, self.lse, self.di,
+                                       self.dq_acc, self.dk, self.dv, s)
             rec(4)
             f.block_attn_bwd_dq_convert(plan, self.dq_acc, self.dq, s)
         else:  # forward only: the backward phases are empty
@@ -358,7 +375,7 @@ def bench_fcp(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     w = workload(args)
-    step = Step(fcp, torch, w, args.coalesce, dev, stream)
+    step = Step(fcp, torch, w, args.coalesce, dev, stream, bwd_band=args.bwd_band)
 
     def barrier():
         if world > 1:

@@ -32,6 +32,7 @@ __all__ = [
     "block_attn_bwd_prologue",
     "block_attn_bwd_tiles",
     "block_attn_bwd_dq_convert",
+    "block_attn_bwd_tiles_banded",
     "reshuffle",
     "FcpAttention",
     "MASK_FULL",
@@ -125,6 +126,10 @@ _SIGNATURES = {
     "fcp_block_attn_merge": (_ST, [_P, _P, _P, _P, _I32, _I32, _P, _P, _P]),
     "fcp_block_attn_bwd_prologue": (_ST, [_P, _P, _P, _I32, _I32, _P, _P, _P]),
     "fcp_bwd_workspace_bytes": (_SZ, [_P, _I32, _I32]),
+    "fcp_plan_set_bwd_band": (_ST, [_P, _I32]),
+    "fcp_plan_bwd_bands": (_ST, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "fcp_bwd_band_workspace_bytes": (_SZ, [_P, _I32, _I32]),
+    "fcp_block_attn_bwd_tiles_banded": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "fcp_block_attn_bwd": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "fcp_block_attn_bwd_tiles": (_ST, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "fcp_block_attn_bwd_dq_convert": (_ST, [_P, _P, _I32, _I32, _P, _P]),
@@ -294,6 +299,22 @@ class Plan:
     def workspace_bytes(self, hq: int, head_dim: int) -> int:
         return int(lib().fcp_bwd_workspace_bytes(self._h, hq, head_dim))
 
+    def set_bwd_band(self, band_rows: int) -> "Plan":
+        """Query bands of the backward (fcp_plan_set_bwd_band): -1 lets the plan choose, 0 none,
+        > 0 rows per band (a multiple of 64). Upload the plan again afterwards."""
+        _check(lib().fcp_plan_set_bwd_band(self._h, int(band_rows)), "fcp_plan_set_bwd_band")
+        return self
+
+    def bwd_bands(self) -> Tuple[int, int]:
+        """(number of backward query bands, rows per band) of the distributed plan."""
+        n, r = _I32(), _I32()
+        _check(lib().fcp_plan_bwd_bands(self._h, ctypes.byref(n), ctypes.byref(r)), "fcp_plan_bwd_bands")
+        return int(n.value), int(r.value)
+
+    def band_workspace_bytes(self, hkv: int, head_dim: int) -> int:
+        """Float32 dK/dV scratch of the banded backward (0 without bands)."""
+        return int(lib().fcp_bwd_band_workspace_bytes(self._h, hkv, head_dim))
+
     def upload(self, d_plan, stream=None) -> None:
         """Copy the device image into ``d_plan`` (a CUDA uint8 tensor of >= device_bytes())."""
         _check(lib().fcp_plan_upload(self._h, _ptr(d_plan), d_plan.numel() * d_plan.element_size(),
@@ -413,6 +434,24 @@ def block_attn_bwd_tiles(plan: Plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk,
                                           _stream(stream)), "fcp_block_attn_bwd_tiles")
 
 
+def block_attn_bwd_tiles_banded(plan: Plan, d_plan, q, k, v, dout, lse, di, dq_acc, dkv_acc, dk, dv,
+                                stream=None) -> None:
+    """The banded tile kernels (fcp_block_attn_bwd_tiles_banded): one launch per query band,
+    dK/dV summed in dkv_acc (uint8 or float32 scratch of Plan.band_workspace_bytes)."""
+    import torch
+
+    hq, T, D = q.shape
+    hkv = k.shape[0]
+    _need(dq_acc, torch.float32, (hq, T, D), "dq_acc")
+    _need(di, torch.float32, (hq, T), "di")
+    if dkv_acc.numel() * dkv_acc.element_size() < plan.band_workspace_bytes(hkv, D):
+        raise ValueError("dkv_acc is smaller than Plan.band_workspace_bytes")
+    _check(lib().fcp_block_attn_bwd_tiles_banded(plan.handle, _ptr(d_plan), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                                 _ptr(lse), _ptr(di), hq, hkv, D, _ptr(dq_acc), _ptr(dkv_acc),
+                                                 _ptr(dk), _ptr(dv), _stream(stream)),
+           "fcp_block_attn_bwd_tiles_banded")
+
+
 def block_attn_bwd_dq_convert(plan: Plan, dq_acc, dq, stream=None) -> None:
     """dq = bf16(dq_acc / sqrt(D)) (fcp_block_attn_bwd_dq_convert)."""
     import torch
@@ -455,17 +494,22 @@ class FcpAttention:
     """A planned batch: the plan, its device image and the partial/workspace buffers, with
     forward (fwd + merge) and backward over the same work list. With ``pipeline=c`` the
     plan is scheduled as the block-level pipeline with coalesce degree c (Plan.schedule) and
-    the forward launches one execution stage at a time before the merge."""
+    the forward launches one execution stage at a time before the merge. ``bwd_band`` sets the
+    backward's query bands (Plan.set_bwd_band; None keeps the plan's own choice); the
+    workspace holds their dK/dV sums, so a plan with bands runs its backward banded."""
 
     def __init__(self, seqlens: Sequence[int], block_size: int, causal: bool, n_workers: int, hq: int, hkv: int,
                  head_dim: int, token_cap: Optional[int] = None, coalesce: int = 1, device="cuda",
-                 backward: bool = True, pipeline: Optional[int] = None):
-        self._recipe = (int(block_size), bool(causal), int(n_workers), token_cap, int(coalesce), pipeline)
+                 backward: bool = True, pipeline: Optional[int] = None, bwd_band: Optional[int] = None):
+        self._recipe = (int(block_size), bool(causal), int(n_workers), token_cap, int(coalesce), pipeline, bwd_band)
         self._setup(self._make_plan(seqlens), hq, hkv, head_dim, device, backward)
 
     def _make_plan(self, seqlens) -> "Plan":
-        block_size, causal, n_workers, token_cap, coalesce, pipeline = self._recipe
-        plan = Plan(seqlens, block_size, causal).distribute(n_workers, token_cap)
+        block_size, causal, n_workers, token_cap, coalesce, pipeline, bwd_band = self._recipe
+        plan = Plan(seqlens, block_size, causal)
+        if bwd_band is not None:
+            plan.set_bwd_band(bwd_band)
+        plan.distribute(n_workers, token_cap)
         if pipeline is not None:
             plan.schedule(pipeline)
         elif coalesce != 1:
@@ -520,7 +564,8 @@ class FcpAttention:
         assert self.part_o.numel() * 4 >= ob and self.part_lse.numel() * 4 >= lb
         self.workspace = None
         if backward:
-            ws = self.plan.workspace_bytes(hq, head_dim)
+            # with query bands, room for their float32 dK/dV sums, so that the backward runs banded
+            ws = self.plan.workspace_bytes(hq, head_dim) + self.plan.band_workspace_bytes(hkv, head_dim)
             self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device)
 
     def forward(self, q, k, v, o=None, lse=None, stream=None):

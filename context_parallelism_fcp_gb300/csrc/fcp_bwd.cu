@@ -20,7 +20,7 @@ fcp_status launch_prologue(int64_t T, const void* o, const void* dout, int hq, i
 fcp_status launch_dq_convert(const float* dq_acc, void* dq, long long n, float scale, cudaStream_t s);
 fcp_status launch_bwd_tiles(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
                             const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
-                            int hq, int hkv, int head_dim, cudaStream_t stream);
+                            int hq, int hkv, int head_dim, float* dk_acc, float* dv_acc, cudaStream_t stream);
 
 namespace {
 
@@ -53,7 +53,8 @@ extern "C" fcp_status fcp_block_attn_bwd_tiles(const fcp_plan* plan, const void*
       !aligned16(dq_acc))
     return FCP_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return launch_bwd_tiles(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, head_dim, s);
+  return launch_bwd_tiles(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, head_dim, nullptr, nullptr,
+                          s);
 }
 
 extern "C" fcp_status fcp_block_attn_bwd_dq_convert(const fcp_plan* plan, const float* dq_acc, int32_t hq,
@@ -88,10 +89,47 @@ extern "C" fcp_status fcp_block_attn_bwd(const fcp_plan* plan, const void* d_pla
                                        align256(size_t(hq) * size_t(T) * size_t(head_dim) * sizeof(float)));
   fcp_status st = launch_prologue(T, o, dout, hq, head_dim, di, dq_acc, s);
   if (st != FCP_OK) return st;
-  st = launch_bwd_tiles(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, head_dim, s);
+  // query bands when the plan has them and the workspace holds their dK/dV sums
+  const size_t base = fcp_bwd_workspace_bytes(plan, hq, head_dim);
+  const size_t band = fcp_bwd_band_workspace_bytes(plan, hkv, head_dim);
+  if (band > 0 && workspace_bytes >= base + band) {
+    float* dkv_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base);
+    st = fcp_block_attn_bwd_tiles_banded(plan, d_plan, q, k, v, dout, lse, di, hq, hkv, head_dim, dq_acc, dkv_acc,
+                                         dk, dv, stream);
+  } else {
+    st = launch_bwd_tiles(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, head_dim, nullptr, nullptr,
+                          s);
+  }
   if (st != FCP_OK) return st;
   return launch_dq_convert(dq_acc, dq, static_cast<long long>(hq) * T * head_dim,
                            static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim))), s);
+}
+
+extern "C" fcp_status fcp_block_attn_bwd_tiles_banded(const fcp_plan* plan, const void* d_plan, const void* q,
+                                                      const void* k, const void* v, const void* dout,
+                                                      const float* lse, const float* di, int32_t hq, int32_t hkv,
+                                                      int32_t head_dim, float* dq_acc, float* dkv_acc, void* dk,
+                                                      void* dv, void* stream) {
+  fcp_status st = check_common(plan, d_plan, hq, hkv, head_dim);
+  if (st != FCP_OK) return st;
+  if (plan->layout.n_bands == 0) return FCP_ERR_STATE;
+  const int64_t T = plan->total_tokens;
+  if (T == 0) return FCP_OK;
+  if (!q || !k || !v || !dout || !lse || !di || !dq_acc || !dkv_acc || !dk || !dv) return FCP_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(dq_acc) || (reinterpret_cast<uintptr_t>(dkv_acc) & 255u) != 0)
+    return FCP_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t half = align256(size_t(hkv) * size_t(T) * size_t(head_dim) * sizeof(float));
+  float* dk_acc = dkv_acc;
+  float* dv_acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dkv_acc) + half);
+  FCP_CUDA_TRY(cudaMemsetAsync(dkv_acc, 0, 2 * half, s), "band accumulators");
+  st = launch_bwd_tiles(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, head_dim, dk_acc, dv_acc, s);
+  if (st != FCP_OK) return st;
+  const long long n = static_cast<long long>(hkv) * T * head_dim;
+  st = launch_dq_convert(dk_acc, dk, n, static_cast<float>(1.0 / std::sqrt(static_cast<double>(head_dim))), s);
+  if (st != FCP_OK) return st;
+  return launch_dq_convert(dv_acc, dv, n, 1.0f, s);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -35,6 +35,7 @@ using namespace dev;
 
 constexpr int kBN = 128;  // key rows per CTA
 constexpr int kBQ = 64;   // query rows per step
+static_assert(kBQ == kBwdStepRows, "the plan's query bands count steps of this many rows");
 constexpr int kStages = 3;
 constexpr int kThreads = 448;
 
@@ -114,6 +115,13 @@ struct Args {
   int hkv, group;
   float scale_log2, scale;
   int* err;
+  // query bands: non-null band_units lists this launch's units (grid = units x KV heads); the
+  // CTA walks only the query steps whose first row lies in [band_lo, band_hi) and adds its dK
+  // and dV (unscaled, float32) into dk_acc / dv_acc instead of writing dk / dv
+  const int* band_units;
+  int band_lo, band_hi;
+  float* dk_acc;
+  float* dv_acc;
 };
 
 template <int D>
@@ -140,9 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int unit_idx = blockIdx.x / a.hkv;
-  const int kvh = blockIdx.x - unit_idx * a.hkv;
-  const BwdUnit unit = a.units[unit_idx];
+  const int slot = blockIdx.x / a.hkv;
+  const int kvh = blockIdx.x - slot * a.hkv;
+  const bool banded = a.band_units != nullptr;
+  const BwdUnit unit = a.units[banded ? a.band_units[slot] : slot];
   const KvSeg seg = a.kvsegs[unit.kvseg];
   const int kt = unit.kv_tile;
   const int kv_row0 = seg.tok0 + kt * kBN;
@@ -187,14 +196,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Steps: for each query head of the group, each item whose key range is this one, each
   // 64-row query step that sees this key tile (a causal diagonal item starts at the step
   // holding the tile's first key). body(step, h, item, qs) returns false to stop.
+  // In a band the CTAs of consecutive key tiles start on different query heads, so that the
+  // CTAs running together add into different dQ rows of the band.
+  auto ceil_steps = [](int rows) { return rows > 0 ? (rows + kBQ - 1) / kBQ : -((-rows) / kBQ); };
   auto for_each_step = [&](auto&& body) -> int {
     int step = 0;
     for (int hh = 0; hh < a.group; ++hh) {
-      const int h = kvh * a.group + hh;
+      const int h = kvh * a.group + (banded ? (hh + kt) % a.group : hh);
       for (int li = seg.list_begin; li < seg.list_end; ++li) {
         const fcp_item itm = a.items[a.kv_items[li]];
-        const int q_end = (itm.q_len + kBQ - 1) / kBQ;
-        const int q_first = itm.mask == FCP_MASK_CAUSAL_DIAG ? (kt * kBN) / kBQ : 0;
+        int q_end = (itm.q_len + kBQ - 1) / kBQ;
+        int q_first = itm.mask == FCP_MASK_CAUSAL_DIAG ? (kt * kBN) / kBQ : 0;
+        if (banded) {
+          q_first = max(q_first, ceil_steps(a.band_lo - itm.q_tok0));
+          q_end = min(q_end, ceil_steps(a.band_hi - itm.q_tok0));
+        }
         for (int qs = q_first; qs < q_end; ++qs, ++step)
           if (!body(step, h, itm, qs)) return step;
       }
@@ -425,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       });
     }
-    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK (bf16)
+    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK (bf16); in a band both
+    // add their unscaled float32 sums into the band accumulators
     if (ok) ok = bwait(bar(B_ACCDONE), 0, abort_flag, a.err, kErrBwdWait + 10);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
@@ -444,7 +461,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = 0u;
         }
-        if (store) {
+        if (store && banded) {
+          // float32 sums over the bands: this CTA owns these rows within the launch
+          float4* acc = reinterpret_cast<float4*>((wg == 0 ? a.dv_acc : a.dk_acc) + row * kD + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 y = acc[e];
+            y.x += __uint_as_float(x[4 * e + 0]);
+            y.y += __uint_as_float(x[4 * e + 1]);
+            y.z += __uint_as_float(x[4 * e + 2]);
+            y.w += __uint_as_float(x[4 * e + 3]);
+            acc[e] = y;
+          }
+        } else if (store) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 pk;
@@ -522,11 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Launch of the backward tile kernel (same contract as fcp_block_attn_bwd_tiles).
+// Launch of the backward tile kernel (same contract as fcp_block_attn_bwd_tiles). With dk_acc
+// and dv_acc (zeroed float32 [Hkv, T, D]) the plan's query bands run as one launch each.
 template <int D>
 fcp_status launch_bwd_tile(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
                            const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
-                           int hq, int hkv, cudaStream_t stream) {
+                           int hq, int hkv, float* dk_acc, float* dv_acc, cudaStream_t stream) {
   using C = TileCfg<D>;
   const DevLayout& L = plan->layout;
   if (L.n_bwd_units == 0) return FCP_OK;
@@ -554,12 +584,32 @@ fcp_status launch_bwd_tile(const fcp_plan* plan, const void* d_plan, const void*
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   a.err = dev_error_word(d_plan);
+  a.band_units = nullptr;
+  a.band_lo = a.band_hi = 0;
+  a.dk_acc = dk_acc;
+  a.dv_acc = dv_acc;
   FCP_CUDA_TRY(cudaFuncSetAttribute(bwd_tile_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                "bwd smem attribute");
-  const long long grid = static_cast<long long>(L.n_bwd_units) * hkv;
-  if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
-  bwd_tile_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
-  FCP_CUDA_TRY(cudaGetLastError(), "bwd launch");
+  if (dk_acc == nullptr) {
+    const long long grid = static_cast<long long>(L.n_bwd_units) * hkv;
+    if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
+    bwd_tile_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
+    FCP_CUDA_TRY(cudaGetLastError(), "bwd launch");
+    return FCP_OK;
+  }
+  if (L.n_bands == 0 || dv_acc == nullptr) return FCP_ERR_STATE;
+  const int* band_units = dev_array<int>(d_plan, L.band_units);
+  for (int32_t b = 0; b < L.n_bands; ++b) {
+    const int32_t n = L.band_begin[b + 1] - L.band_begin[b];
+    if (n == 0) continue;
+    a.band_units = band_units + L.band_begin[b];
+    a.band_lo = b * L.band_rows;
+    a.band_hi = static_cast<int>(std::min<int64_t>(T, int64_t(b + 1) * L.band_rows));
+    const long long grid = static_cast<long long>(n) * hkv;
+    if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
+    bwd_tile_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
+    FCP_CUDA_TRY(cudaGetLastError(), "bwd band launch");
+  }
   return FCP_OK;
 }
 
@@ -567,10 +617,11 @@ fcp_status launch_bwd_tile(const fcp_plan* plan, const void* d_plan, const void*
 
 fcp_status launch_bwd_tiles(const fcp_plan* plan, const void* d_plan, const void* q, const void* k, const void* v,
                             const void* dout, const float* lse, const float* di, float* dq_acc, void* dk, void* dv,
-                            int hq, int hkv, int head_dim, cudaStream_t stream) {
+                            int hq, int hkv, int head_dim, float* dk_acc, float* dv_acc, cudaStream_t stream) {
   if (head_dim == 128)
-    return launch_bwd_tile<128>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, stream);
-  return launch_bwd_tile<64>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, stream);
+    return launch_bwd_tile<128>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, dk_acc, dv_acc,
+                                stream);
+  return launch_bwd_tile<64>(plan, d_plan, q, k, v, dout, lse, di, dq_acc, dk, dv, hq, hkv, dk_acc, dv_acc, stream);
 }
 
 }  // namespace fcp

@@ -15,6 +15,12 @@ namespace fcp {
 // single-CTA tcgen05.mma and the number of TMEM lanes, so one thread owns one row.
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
+// Query rows of one backward step (the N of the backward's S^T and dP^T MMAs).
+constexpr int kBwdStepRows = 64;
+// Query bands of the backward: off below this many tokens unless a plan asks for them, and
+// this many rows per band when on by default.
+constexpr int64_t kAutoBandMinTokens = 131072;
+constexpr int32_t kAutoBandRows = 4096;
 
 // A query range with its runs (consecutive in the run list): what the merge reduces.
 // A query range: its tokens, how many runs reduce it and the first of its partial rows.
@@ -61,6 +67,12 @@ struct DevLayout {
   int32_t max_runs_per_qseg = 0;
   // forward units of execution stage s: [stage_unit_begin[s], stage_unit_begin[s + 1])
   std::vector<int32_t> stage_unit_begin;
+  // Backward query bands (0 rows: none). Band k covers the query steps whose first row lies
+  // in [k * band_rows, (k + 1) * band_rows); its units are band_units[band_begin[k],
+  // band_begin[k + 1]) (indices into bwd_units, in their order).
+  size_t band_units = 0;
+  int32_t band_rows = 0, n_bands = 0, n_band_units = 0;
+  std::vector<int32_t> band_begin;
 };
 
 // Device error codes written into DevHeader::error (kernel id * 16 + wait id).
@@ -104,6 +116,9 @@ struct fcp_plan {
   bool solved = false;
   std::vector<fcp_transfer> transfers;
   int32_t n_stages = 0;
+
+  // Backward query bands: -1 chooses (on for long batches), 0 off, > 0 rows per band.
+  int32_t bwd_band_rows = -1;
 
   // Host copy of the device image, rebuilt after distribute/coalesce.
   std::vector<uint8_t> image;

@@ -189,6 +189,35 @@ fcp_status build_image(fcp_plan* p) {
   bwd_units.reserve(bu.size());
   for (auto& x : bu) bwd_units.push_back(x.second);
 
+  // Backward query bands: band k lists the units with a query step whose first row lies in
+  // [k * R, (k + 1) * R). A unit's steps over one item are the 64-row steps from the one
+  // holding the key tile's first key (causal diagonal) or 0 to the end of the item's rows.
+  const int32_t R = p->bwd_band_rows > 0 ? p->bwd_band_rows
+                    : (p->bwd_band_rows < 0 && p->total_tokens >= kAutoBandMinTokens ? kAutoBandRows : 0);
+  std::vector<int32_t> band_begin, band_units;
+  if (R > 0 && !bwd_units.empty()) {
+    std::vector<std::vector<int32_t>> per(static_cast<size_t>(ceil_div(p->total_tokens, R)));
+    for (int32_t u = 0; u < static_cast<int32_t>(bwd_units.size()); ++u) {
+      const KvSeg& sg = kvsegs[bwd_units[u].kvseg];
+      const int32_t kt = bwd_units[u].kv_tile;
+      for (int32_t i = sg.list_begin; i < sg.list_end; ++i) {
+        const fcp_item& it = p->items[kv_items[i]];
+        const int32_t q_first = it.mask == FCP_MASK_CAUSAL_DIAG ? (kt * kTileN) / kBwdStepRows : 0;
+        const int32_t q_end = ceil_div(it.q_len, kBwdStepRows);
+        if (q_first >= q_end) continue;
+        const int64_t b0 = (static_cast<int64_t>(it.q_tok0) + int64_t(q_first) * kBwdStepRows) / R;
+        const int64_t b1 = (static_cast<int64_t>(it.q_tok0) + int64_t(q_end - 1) * kBwdStepRows) / R;
+        for (int64_t b = b0; b <= b1; ++b)
+          if (per[b].empty() || per[b].back() != u) per[b].push_back(u);
+      }
+    }
+    band_begin.push_back(0);
+    for (const auto& v : per) {
+      band_units.insert(band_units.end(), v.begin(), v.end());
+      band_begin.push_back(static_cast<int32_t>(band_units.size()));
+    }
+  }
+
   // workers' token layout: worker w's blocks in ascending id, their segments in order
   std::vector<int32_t> worker_order;
   worker_order.reserve(static_cast<size_t>(p->total_tokens));
@@ -220,6 +249,8 @@ fcp_status build_image(fcp_plan* p) {
   off = align256(off + kv_items.size() * sizeof(int32_t));
   L.bwd_units = off;
   off = align256(off + bwd_units.size() * sizeof(BwdUnit));
+  L.band_units = off;
+  off = align256(off + band_units.size() * sizeof(int32_t));
   L.total = off;
   L.n_qsegs = static_cast<int32_t>(qsegs.size());
   L.n_fwd_units = static_cast<int32_t>(fwd_units.size());
@@ -228,6 +259,10 @@ fcp_status build_image(fcp_plan* p) {
   L.n_bwd_units = static_cast<int32_t>(bwd_units.size());
   L.max_runs_per_qseg = max_runs;
   L.stage_unit_begin = std::move(stage_begin);
+  L.band_rows = band_begin.empty() ? 0 : R;
+  L.n_bands = band_begin.empty() ? 0 : static_cast<int32_t>(band_begin.size()) - 1;
+  L.n_band_units = static_cast<int32_t>(band_units.size());
+  L.band_begin = std::move(band_begin);
 
   for (const TokPart& tp : tok2part)
     if (tp.count <= 0) return FCP_ERR_STATE;  // every token must belong to exactly one query range
@@ -241,6 +276,7 @@ fcp_status build_image(fcp_plan* p) {
   put(p->image, L.kvsegs, kvsegs);
   put(p->image, L.kv_items, kv_items);
   put(p->image, L.bwd_units, bwd_units);
+  put(p->image, L.band_units, band_units);
   p->layout = L;
   return FCP_OK;
 }
@@ -604,6 +640,25 @@ fcp_status fcp_plan_query(const fcp_plan* p, fcp_plan_view* v) {
   return FCP_OK;
 }
 
+fcp_status fcp_plan_set_bwd_band(fcp_plan* p, int32_t band_rows) {
+  if (p == nullptr || band_rows < -1 || (band_rows > 0 && band_rows % kBwdStepRows != 0)) return FCP_ERR_INVALID;
+  p->bwd_band_rows = band_rows;
+  if (!p->distributed) return FCP_OK;  // applied when the plan is distributed
+  if (const fcp_status st = build_image(p); st != FCP_OK) {
+    p->distributed = false;
+    return st;
+  }
+  return FCP_OK;
+}
+
+fcp_status fcp_plan_bwd_bands(const fcp_plan* p, int32_t* n_bands, int32_t* band_rows) {
+  if (p == nullptr || n_bands == nullptr || band_rows == nullptr) return FCP_ERR_INVALID;
+  if (!p->distributed) return FCP_ERR_STATE;
+  *n_bands = p->layout.n_bands;
+  *band_rows = p->layout.band_rows;
+  return FCP_OK;
+}
+
 size_t fcp_plan_device_bytes(const fcp_plan* p) {
   if (p == nullptr || !p->distributed) return 0;
   return p->layout.total;
@@ -623,6 +678,11 @@ size_t fcp_bwd_workspace_bytes(const fcp_plan* p, int32_t hq, int32_t head_dim) 
   if (p == nullptr || hq <= 0 || head_dim <= 0) return 0;
   const size_t T = size_t(p->total_tokens);
   return align256(size_t(hq) * T * size_t(head_dim) * sizeof(float)) + align256(size_t(hq) * T * sizeof(float));
+}
+
+size_t fcp_bwd_band_workspace_bytes(const fcp_plan* p, int32_t hkv, int32_t head_dim) {
+  if (p == nullptr || hkv <= 0 || head_dim <= 0 || !p->distributed || p->layout.n_bands == 0) return 0;
+  return 2 * align256(size_t(hkv) * size_t(p->total_tokens) * size_t(head_dim) * sizeof(float));
 }
 
 void fcp_plan_free(fcp_plan* p) { delete p; }

@@ -1,8 +1,8 @@
 // Host-side validation of a distributed plan and of its device image: every index the
 // kernels follow (items, runs, partial rows, token-to-partial records, forward and backward
-// tile units, the reversed work list, the workers' token order) is checked against the
-// token count, the sequence boundaries and the other arrays, so a plan that passes can be
-// uploaded without any kernel reading or writing outside its buffers.
+// tile units, the reversed work list, the backward's query bands, the workers' token order)
+// is checked against the token count, the sequence boundaries and the other arrays, so a
+// plan that passes can be uploaded without any kernel reading or writing outside its buffers.
 //
 // The coverage check restates the work list's contract ("Unleashing Scalable Context
 // Parallelism for Foundation Models Pre-Training via FCP", Section 2.2 with the block pairs
@@ -189,6 +189,40 @@ void validate(const fcp_plan* p) {
     require(bu.kv_tile >= 0 && bu.kv_tile < static_cast<int32_t>(bwd_seen[bu.kvseg].size()), "backward unit tile");
     require(!bwd_seen[bu.kvseg][bu.kv_tile], "backward unit listed twice");
     bwd_seen[bu.kvseg][bu.kv_tile] = 1;
+  }
+
+  // query bands: every (unit, band) pair where the unit has a 64-row step starting in the band
+  // is listed exactly once, and nothing else is
+  if (L.n_bands == 0) {
+    require(L.n_band_units == 0 && L.band_begin.empty(), "band lists without bands");
+    return;
+  }
+  require(L.band_rows > 0 && L.band_rows % kBwdStepRows == 0, "band size");
+  require(static_cast<int64_t>(L.n_bands) == ceil_div64(T, L.band_rows), "band count");
+  const auto& bb = L.band_begin;
+  require(static_cast<int32_t>(bb.size()) == L.n_bands + 1 && bb.front() == 0 && bb.back() == L.n_band_units,
+          "band offsets");
+  const auto band_units = image_array<int32_t>(p, L.band_units, static_cast<size_t>(L.n_band_units));
+  std::vector<std::vector<int32_t>> want(static_cast<size_t>(L.n_bands));
+  for (int32_t u = 0; u < L.n_bwd_units; ++u) {
+    const KvSeg& ks = kvsegs[bwd[u].kvseg];
+    for (int32_t li = ks.list_begin; li < ks.list_end; ++li) {
+      const fcp_item& it = p->items[kv_items[li]];
+      const int64_t first = it.mask == FCP_MASK_CAUSAL_DIAG ? (int64_t(bwd[u].kv_tile) * kTileN) / kBwdStepRows : 0;
+      for (int64_t qs = first; qs < ceil_div64(it.q_len, kBwdStepRows); ++qs) {
+        auto& w = want[(it.q_tok0 + qs * kBwdStepRows) / L.band_rows];
+        if (w.empty() || w.back() != u) w.push_back(u);
+      }
+    }
+  }
+  for (int32_t b = 0; b < L.n_bands; ++b) {
+    require(bb[b] <= bb[b + 1], "band offsets");
+    std::vector<int32_t> got(band_units.begin() + bb[b], band_units.begin() + bb[b + 1]);
+    for (int32_t u : got) require(u >= 0 && u < L.n_bwd_units, "band unit out of range");
+    std::sort(got.begin(), got.end());
+    require(std::adjacent_find(got.begin(), got.end()) == got.end(), "band unit listed twice");
+    std::sort(want[b].begin(), want[b].end());
+    require(got == want[b], "band unit list differs from the units with steps in the band");
   }
 }
 

@@ -260,13 +260,39 @@ fcp_status fcp_block_attn_bwd_prologue(const fcp_plan* plan, const void* o, cons
  * the float32 Di [Hq, T] (each 256-byte aligned). */
 size_t fcp_bwd_workspace_bytes(const fcp_plan* plan, int32_t hq, int32_t head_dim);
 
+/* Query bands of the backward (no counterpart on the pages; a schedule of the backward on one
+ * GPU). With bands, the backward runs as one launch per band of band_rows query rows: each
+ * launch walks only the query steps whose first row lies in its band, so the dQ rows that all
+ * running CTAs add into, and the Q/dO/LSE/Di rows they read, stay within one band and in L2;
+ * dK and dV are summed over the bands in float32 scratch (fcp_bwd_band_workspace_bytes) and
+ * written as bf16 at the end. band_rows: -1 lets the plan choose (4096 for batches of at least
+ * 131072 tokens, else none; the default), 0 none, > 0 rows per band (a multiple of 64).
+ * Measured on one causal sequence, 64/8 heads, D = 128 (backward ms): 131072 tokens 761 with
+ * none, 697 / 694 / 727 / 791 with 2048 / 4096 / 8192 / 16384-row bands; 524288 tokens 13664
+ * with none, 14775 / 12387 / 11450-11611 / 11388 / 12804 with 1024 / 2048 / 4096 / 8192 /
+ * 16384; 65536 tokens 148 with none, 179 with 8192; 32768 tokens 35.6 with none, 40.1 with
+ * 2048.
+ * May be called before or after fcp_distribute; a distributed plan's device image is rebuilt
+ * (upload it again). Errors: FCP_ERR_INVALID. */
+fcp_status fcp_plan_set_bwd_band(fcp_plan* plan, int32_t band_rows);
+
+/* The bands of a distributed plan: *n_bands (0: none) and *band_rows. FCP_ERR_STATE if the
+ * plan is not distributed. */
+fcp_status fcp_plan_bwd_bands(const fcp_plan* plan, int32_t* n_bands, int32_t* band_rows);
+
+/* Float32 scratch for dK and dV summed over the query bands ([2][Hkv, T, D], each half
+ * 256-byte aligned), 0 if the plan has no bands. fcp_block_attn_bwd runs banded when the plan
+ * has bands and its workspace holds fcp_bwd_workspace_bytes + this many bytes. */
+size_t fcp_bwd_band_workspace_bytes(const fcp_plan* plan, int32_t hkv, int32_t head_dim);
+
 /* Backward over the same work list (the exact gradient of the Section 2.2 attention; the
  * pages implement a backward but describe only the forward): with P = exp(S*scale - lse),
  * dV = sum P^T dO, dP = dO V^T, dS = P * (dP - Di), dQ = scale dS K, dK = scale dS^T Q,
  * KV gradients summed over the query heads of their group. lse is the merged LSE from
  * fcp_block_attn_merge, o the merged output. Launches the prologue, the tile kernel and
  * the dQ conversion on `stream`. dq [Hq,T,D], dk and dv [Hkv,T,D] bf16 outputs; workspace
- * of fcp_bwd_workspace_bytes, 256-byte aligned. */
+ * of fcp_bwd_workspace_bytes, 256-byte aligned, to which a plan with query bands adds
+ * fcp_bwd_band_workspace_bytes to run banded (with less it runs in one launch). */
 fcp_status fcp_block_attn_bwd(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
                               const void* v, const void* o, const void* dout, const float* lse, int32_t hq,
                               int32_t hkv, int32_t head_dim, void* dq, void* dk, void* dv, void* workspace,
@@ -279,6 +305,16 @@ fcp_status fcp_block_attn_bwd_tiles(const fcp_plan* plan, const void* d_plan, co
                                     const void* v, const void* dout, const float* lse, const float* di,
                                     int32_t hq, int32_t hkv, int32_t head_dim, float* dq_acc, void* dk, void* dv,
                                     void* stream);
+
+/* The banded tile kernels of fcp_block_attn_bwd alone (a plan with query bands): zeroes
+ * dkv_acc (float32 [2][Hkv, T, D] of fcp_bwd_band_workspace_bytes, 256-byte aligned), launches
+ * the tile kernel once per band, accumulating dQ / scale into dq_acc as
+ * fcp_block_attn_bwd_tiles does and dK, dV into dkv_acc, then writes dk, dv [Hkv, T, D] bf16.
+ * FCP_ERR_STATE if the plan has no bands. */
+fcp_status fcp_block_attn_bwd_tiles_banded(const fcp_plan* plan, const void* d_plan, const void* q, const void* k,
+                                           const void* v, const void* dout, const float* lse, const float* di,
+                                           int32_t hq, int32_t hkv, int32_t head_dim, float* dq_acc,
+                                           float* dkv_acc, void* dk, void* dv, void* stream);
 
 /* The last step of fcp_block_attn_bwd alone: dq = bf16(dq_acc / sqrt(D)) over [Hq, T, D]. */
 fcp_status fcp_block_attn_bwd_dq_convert(const fcp_plan* plan, const float* dq_acc, int32_t hq, int32_t head_dim,

@@ -35,14 +35,14 @@ def _record(where, name, emax, bmax, emean=None, bmean=None):
                    None if emean is None else float(emean), None if bmean is None else float(bmean)))
 
 
-def run_path(fcp, w: W.Workload, coalesce=None, backward=None, device="cuda", pipeline=None):
+def run_path(fcp, w: W.Workload, coalesce=None, backward=None, device="cuda", pipeline=None, bwd_band=None):
     backward = w.backward if backward is None else backward
     dev = torch.device(device)
     q, k, v = W.make_qkv(w, device=dev)
     do = W.make_dout(w, device=dev) if backward else None
     att = fcp.FcpAttention(w.seqlens, w.block_size, w.causal, w.n_workers, w.hq, w.hkv, w.head_dim,
                            token_cap=w.token_cap, coalesce=coalesce or w.coalesce, device=dev, backward=backward,
-                           pipeline=pipeline)
+                           pipeline=pipeline, bwd_band=bwd_band)
     o, lse = att.forward(q, k, v)
     grads = att.backward(q, k, v, o, lse, do) if backward else None
     torch.cuda.synchronize()

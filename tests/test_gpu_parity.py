@@ -32,6 +32,20 @@ def test_forward_and_backward_small(fcp, w):
         U.check_grad(name, U.np64(got), ref, w.name)
 
 
+@pytest.mark.parametrize("band", [64, 192, 512])
+@pytest.mark.parametrize("w", W.small_cases(), ids=lambda w: w.name)
+def test_backward_in_query_bands_small(fcp, w, band):
+    """The backward run as one launch per query band (dK/dV summed over the bands in float32)
+    against the oracle, element by element; bands of one step, of a ragged 3 steps and of
+    several key tiles."""
+    r = U.run_path(fcp, w, bwd_band=band)
+    n, rows = r["att"].plan.bwd_bands()
+    assert rows == band and n == -(-w.total_tokens // band)
+    rdq, rdk, rdv = A.attention_backward(r["q"], r["k"], r["v"], r["do"], w.seqlens, w.causal)
+    for name, got, ref in zip(("dq", "dk", "dv"), r["grads"], (rdq, rdk, rdv)):
+        U.check_grad(name, U.np64(got), ref, f"{w.name} band {band}")
+
+
 @pytest.mark.parametrize("c", [1, 2, 16])
 def test_coalesce_degree_does_not_change_the_result(fcp, c):
     w = W.Workload("mixed small", [1500, 40, 700, 2600], 512, 8, 2, 128, 3, True)
@@ -238,18 +252,22 @@ def test_causal_mixed_all_rows(fcp):
 _LONG_ACC = {}
 
 
-@pytest.mark.parametrize("b,c", [(4096, 16), (1024, 1)], ids=["b4096 c16", "b1024 c1"])
-def test_backward_long_accumulation_all_key_rows(fcp, b, c):
+@pytest.mark.parametrize("b,c,band", [(4096, 16, 0), (1024, 1, 0), (4096, 16, 2048)],
+                         ids=["b4096 c16", "b1024 c1", "b4096 c16 bands 2048"])
+def test_backward_long_accumulation_all_key_rows(fcp, b, c, band):
     """dK and dV of every key row, and dQ of every query row, of two KV-head groups of a
     16384-token causal sequence (64/8 heads, D = 128) against the oracle's whole-group
     gradient: at 4096-token blocks with coalesce degree 16 (the benchmark's launch
     configuration) and at 1024-token blocks with one partial per pair. The gradient of an
     early key sums over up to 16384 queries of each of the group's 8 heads: two thousand
-    64-row steps of one backward CTA, over several query blocks and items."""
+    64-row steps of one backward CTA, over several query blocks and items. The third case runs
+    the backward in query bands of 2048 rows (one launch per band, dK/dV summed over eight
+    bands in float32)."""
     L = 16384
     w = W.Workload(f"causal 16k b={b}", [L], b, 64, 8, 128, max(1, L // b // 2), True, token_cap=2 * b,
                    coalesce=c)
-    r = U.run_path(fcp, w)
+    r = U.run_path(fcp, w, bwd_band=band)
+    assert r["att"].plan.bwd_bands()[1] == band
     G = w.hq // w.hkv
     groups = (3, 7)
     q, k, v, do = (r[n].detach().cpu() for n in ("q", "k", "v", "do"))
@@ -265,7 +283,7 @@ def test_backward_long_accumulation_all_key_rows(fcp, b, c):
         _LONG_ACC.update(inputs=fingerprint, ref=ref)
     dq, dk, dv = r["grads"]
     for g, (rdq, rdk, rdv) in zip(groups, _LONG_ACC["ref"]):
-        where = f"b={b} c={c} group {g}"
+        where = f"b={b} c={c} band={band} group {g}"
         U.check_grad("dk", U.np64(dk[g]), rdk, where)
         U.check_grad("dv", U.np64(dv[g]), rdv, where)
         U.check_grad("dq", U.np64(dq[g * G:(g + 1) * G]), rdq, where)
