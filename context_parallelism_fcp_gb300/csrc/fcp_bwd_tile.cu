@@ -124,7 +124,7 @@ struct Args {
   float* dv_acc;
 };
 
-template <int D>
+template <int D, bool kBanded>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -150,8 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int slot = blockIdx.x / a.hkv;
   const int kvh = blockIdx.x - slot * a.hkv;
-  const bool banded = a.band_units != nullptr;
-  const BwdUnit unit = a.units[banded ? a.band_units[slot] : slot];
+  // kBanded: one launch of a banded backward (a.band_units lists its units)
+  const BwdUnit unit = a.units[kBanded ? a.band_units[slot] : slot];
   const KvSeg seg = a.kvsegs[unit.kvseg];
   const int kt = unit.kv_tile;
   const int kv_row0 = seg.tok0 + kt * kBN;
@@ -202,12 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto for_each_step = [&](auto&& body) -> int {
     int step = 0;
     for (int hh = 0; hh < a.group; ++hh) {
-      const int h = kvh * a.group + (banded ? (hh + kt) % a.group : hh);
+      const int h = kvh * a.group + (kBanded ? (hh + kt) % a.group : hh);
       for (int li = seg.list_begin; li < seg.list_end; ++li) {
         const fcp_item itm = a.items[a.kv_items[li]];
         int q_end = (itm.q_len + kBQ - 1) / kBQ;
         int q_first = itm.mask == FCP_MASK_CAUSAL_DIAG ? (kt * kBN) / kBQ : 0;
-        if (banded) {
+        if constexpr (kBanded) {
           q_first = max(q_first, ceil_steps(a.band_lo - itm.q_tok0));
           q_end = min(q_end, ceil_steps(a.band_hi - itm.q_tok0));
         }
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = 0u;
         }
-        if (store && banded) {
+        if (kBanded && store) {
           // float32 sums over the bands: this CTA owns these rows within the launch
           float4* acc = reinterpret_cast<float4*>((wg == 0 ? a.dv_acc : a.dk_acc) + row * kD + c * 32);
 #pragma unroll
@@ -588,12 +588,17 @@ fcp_status launch_bwd_tile(const fcp_plan* plan, const void* d_plan, const void*
   a.band_lo = a.band_hi = 0;
   a.dk_acc = dk_acc;
   a.dv_acc = dv_acc;
-  FCP_CUDA_TRY(cudaFuncSetAttribute(bwd_tile_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
+  FCP_CUDA_TRY(cudaFuncSetAttribute(bwd_tile_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmemBytes),
+               "bwd smem attribute");
+  FCP_CUDA_TRY(cudaFuncSetAttribute(bwd_tile_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmemBytes),
                "bwd smem attribute");
   if (dk_acc == nullptr) {
     const long long grid = static_cast<long long>(L.n_bwd_units) * hkv;
     if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
-    bwd_tile_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
+    bwd_tile_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo,
+                                                                                                 mdq, a);
     FCP_CUDA_TRY(cudaGetLastError(), "bwd launch");
     return FCP_OK;
   }
@@ -607,7 +612,8 @@ fcp_status launch_bwd_tile(const fcp_plan* plan, const void* d_plan, const void*
     a.band_hi = static_cast<int>(std::min<int64_t>(T, int64_t(b + 1) * L.band_rows));
     const long long grid = static_cast<long long>(n) * hkv;
     if (grid > 0x7fffffffLL) return FCP_ERR_UNSUPPORTED;
-    bwd_tile_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a);
+    bwd_tile_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq,
+                                                                                                a);
     FCP_CUDA_TRY(cudaGetLastError(), "bwd band launch");
   }
   return FCP_OK;
