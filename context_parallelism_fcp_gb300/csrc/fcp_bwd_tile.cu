@@ -196,13 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Steps: for each query head of the group, each item whose key range is this one, each
   // 64-row query step that sees this key tile (a causal diagonal item starts at the step
   // holding the tile's first key). body(step, h, item, qs) returns false to stop.
-  // In a band the CTAs of consecutive key tiles start on different query heads, so that the
-  // CTAs running together add into different dQ rows of the band.
+  // (In a band every CTA still walks the group's heads in order: the CTAs of one KV head then
+  // read the same Q/dO rows at about the same time, which measured 5-9% faster than starting
+  // consecutive key tiles on different heads.)
   auto ceil_steps = [](int rows) { return rows > 0 ? (rows + kBQ - 1) / kBQ : -((-rows) / kBQ); };
   auto for_each_step = [&](auto&& body) -> int {
     int step = 0;
     for (int hh = 0; hh < a.group; ++hh) {
-      const int h = kvh * a.group + (kBanded ? (hh + kt) % a.group : hh);
+      const int h = kvh * a.group + hh;
       for (int li = seg.list_begin; li < seg.list_end; ++li) {
         const fcp_item itm = a.items[a.kv_items[li]];
         int q_end = (itm.q_len + kBQ - 1) / kBQ;

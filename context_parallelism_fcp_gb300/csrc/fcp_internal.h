@@ -20,7 +20,7 @@ constexpr int kBwdStepRows = 64;
 // Query bands of the backward: off below this many tokens unless a plan asks for them, and
 // this many rows per band when on by default.
 constexpr int64_t kAutoBandMinTokens = 131072;
-constexpr int32_t kAutoBandRows = 4096;
+constexpr int32_t kAutoBandRows = 16384;
 
 // A query range with its runs (consecutive in the run list): what the merge reduces.
 // A query range: its tokens, how many runs reduce it and the first of its partial rows.

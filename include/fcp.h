@@ -262,16 +262,16 @@ size_t fcp_bwd_workspace_bytes(const fcp_plan* plan, int32_t hq, int32_t head_di
 
 /* Query bands of the backward (no counterpart on the pages; a schedule of the backward on one
  * GPU). With bands, the backward runs as one launch per band of band_rows query rows: each
- * launch walks only the query steps whose first row lies in its band, so the dQ rows that all
- * running CTAs add into, and the Q/dO/LSE/Di rows they read, stay within one band and in L2;
- * dK and dV are summed over the bands in float32 scratch (fcp_bwd_band_workspace_bytes) and
- * written as bf16 at the end. band_rows: -1 lets the plan choose (4096 for batches of at least
+ * launch walks only the query steps whose first row lies in its band, so the CTAs running
+ * together walk the same slice of query rows head by head and share, while they are in L2, the
+ * dQ rows they add into and the Q/dO/LSE/Di rows they read; dK and dV are summed over the bands in float32 scratch (fcp_bwd_band_workspace_bytes) and
+ * written as bf16 at the end. band_rows: -1 lets the plan choose (16384 for batches of at least
  * 131072 tokens, else none; the default), 0 none, > 0 rows per band (a multiple of 64).
- * Measured on one causal sequence, 64/8 heads, D = 128 (backward ms): 131072 tokens 761 with
- * none, 697 / 694 / 727 / 791 with 2048 / 4096 / 8192 / 16384-row bands; 524288 tokens 13664
- * with none, 14775 / 12387 / 11450-11611 / 11388 / 12804 with 1024 / 2048 / 4096 / 8192 /
- * 16384; 65536 tokens 148 with none, 179 with 8192; 32768 tokens 35.6 with none, 40.1 with
- * 2048.
+ * Measured on one causal sequence, 64/8 heads, D = 128 (backward ms, one box per row):
+ * 524288 tokens 13664 with none, 12181 / 10813 / 10234 with 2048 / 4096 / 8192-row bands, and
+ * on another box 10397 / 9969 / 11082 with 8192 / 16384 / 32768; 131072 tokens 761-791 with
+ * none, 615-617 with 8192 and 605-606 with 16384; 65536 tokens 150.0-150.2 with none and
+ * 148.9-149.0 with 16384; 32768 tokens 36.74-36.80 with none and 36.66-36.88 with 16384.
  * May be called before or after fcp_distribute; a distributed plan's device image is rebuilt
  * (upload it again). Errors: FCP_ERR_INVALID. */
 fcp_status fcp_plan_set_bwd_band(fcp_plan* plan, int32_t band_rows);

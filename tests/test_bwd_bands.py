@@ -18,7 +18,7 @@ def _plan(fcp, w, band=None, coalesce=16):
 def test_default_bands_only_for_long_batches(fcp):
     assert _plan(fcp, W.block_sweep(4096)).bwd_bands() == (0, 0)  # 32768 tokens
     p = _plan(fcp, W.long_causal())  # 524288 tokens
-    assert p.bwd_bands() == (524288 // 4096, 4096)
+    assert p.bwd_bands() == (524288 // 16384, 16384)
     p.validate()
 
 
