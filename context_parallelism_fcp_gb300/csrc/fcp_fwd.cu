@@ -81,8 +81,14 @@ struct FwdCfg {
   static constexpr int kK = 2 * kTileBytes;
   static constexpr int kV = 4 * kTileBytes;
   static constexpr int kBar = 6 * kTileBytes;
+  // epilogue staging: one [32 rows][32 float32] block per softmax warp
+  static constexpr int kStage = kBar + kBarArea;
+  static constexpr int kStageBytes = 8 * 32 * 32 * 4;
+  static constexpr int kEnd = kStage + kStageBytes;
   // at least half the SM's shared memory, so one CTA per SM holds all 512 TMEM columns
-  static constexpr int kSmemBytes = (kBar + kBarArea) > 118 * 1024 ? (kBar + kBarArea) : 118 * 1024;
+  static constexpr int kSmemBytes = kEnd > 118 * 1024 ? kEnd : 118 * 1024;
+  static_assert(kStage % 16 == 0, "16-byte aligned staging");
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
   static constexpr uint32_t kIdescS = idesc_bf16(kTileM, kTileN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kTileM, D, false, true);
 };
@@ -511,11 +517,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int qrow = qt * kTileM + r;
-      const bool store = qrow < T.q_len && (t == 0 || T.has_h1);
+      const bool head_ok = t == 0 || T.has_h1;
+      const bool store = qrow < T.q_len && head_ok;
       const int h = t ? T.h1 : T.h0;
       const long long prow = static_cast<long long>(h) * a.part_rows + T.part_row0 + qrow;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D);
+      // Each 32-column slice of the warp's 32 rows goes through a shared [32][32] float32
+      // block (16-byte slots XOR-swizzled by row, so neither side has bank conflicts) and
+      // leaves as stores that write four whole 128-byte row segments per instruction, instead
+      // of one 16-byte piece of 32 different rows.
+      float4* stg = reinterpret_cast<float4*>(smem + C::kStage + warp * 4096);
+      const int wrow0 = qt * kTileM + (warp & 3) * 32;   // the warp's first row in the run
+      const int sub = lane >> 3, slot = lane & 7;        // store side: row sub + 4i, slot
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -524,13 +537,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tc_fence_before();
           mbar_arrive_warp(bar(B_OFREE + t));
         }
-        if (store) {
+        if (c > 0) __syncwarp();  // the previous slice has been read out of the block
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[c * 8 + e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
-                                         __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+        for (int e = 0; e < 8; ++e)
+          stg[lane * 8 + (e ^ (lane & 7))] =
+              make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
+                          __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+        __syncwarp();
+        if (head_ok) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + sub;
+            if (wrow0 + rr < T.q_len) {
+              const long long orow = static_cast<long long>(h) * a.part_rows + T.part_row0 + wrow0 + rr;
+              reinterpret_cast<float4*>(a.part_o + orow * D)[c * 8 + slot] = stg[rr * 8 + (slot ^ (rr & 7))];
+            }
+          }
         }
       }
+      __syncwarp();  // the block is free for the next tile's epilogue
       if (store) a.part_lse[prow] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
