@@ -62,10 +62,9 @@ inline fcp_status make_bf16_map(CUtensorMap* map, const void* base, int heads, i
   return FCP_OK;
 }
 
-// Tensor map over a contiguous float32 tensor [heads, T, 128] with box {128, rows, 1}, no
-// swizzle: one box is `rows` tokens x 128 channels (512 bytes per row).
-// Float32 [heads, T, D] tensor (D innermost), boxes of D x rows, no swizzle (the dQ
-// accumulator that the backward's reduce-adds target).
+// Tensor map over a contiguous float32 tensor [heads, T, D] (D innermost) with box
+// {D, rows, 1}, no swizzle: one box is `rows` tokens x D channels (the dQ accumulator that
+// the backward's reduce-adds target).
 inline fcp_status make_f32_map(CUtensorMap* map, const void* base, int heads, int64_t T, int D, int rows) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) {
