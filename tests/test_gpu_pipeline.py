@@ -3,7 +3,6 @@ Foundation Models Pre-Training via FCP", Section 4.2, Figure 7): the forward lau
 execution stage at a time (fcp_block_attn_fwd_stage), then merged, against the float64
 oracle; the stages together write exactly the partials of one whole launch; the backward
 over the scheduled work list."""
-import numpy as np
 import pytest
 import torch
 

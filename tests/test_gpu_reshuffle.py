@@ -1,6 +1,5 @@
 """GPU parity of the transparent reshuffle (permutation between the user's and the workers'
 token layouts) against the oracle's worker order: bit-exact gather and round trip."""
-import numpy as np
 import pytest
 import torch
 
