@@ -252,9 +252,10 @@ def test_causal_mixed_all_rows(fcp):
 _LONG_ACC = {}
 
 
-@pytest.mark.parametrize("b,c,band", [(4096, 16, 0), (1024, 1, 0), (4096, 16, 2048)],
-                         ids=["b4096 c16", "b1024 c1", "b4096 c16 bands 2048"])
-def test_backward_long_accumulation_all_key_rows(fcp, b, c, band):
+@pytest.mark.parametrize("b,c,band,head_dim", [(4096, 16, 0, 128), (1024, 1, 0, 128), (4096, 16, 2048, 128),
+                                               (4096, 16, 0, 64)],
+                         ids=["b4096 c16", "b1024 c1", "b4096 c16 bands 2048", "b4096 c16 D64"])
+def test_backward_long_accumulation_all_key_rows(fcp, b, c, band, head_dim):
     """dK and dV of every key row, and dQ of every query row, of two KV-head groups of a
     16384-token causal sequence (64/8 heads, D = 128) against the oracle's whole-group
     gradient: at 4096-token blocks with coalesce degree 16 (the benchmark's launch
@@ -262,14 +263,16 @@ def test_backward_long_accumulation_all_key_rows(fcp, b, c, band):
     early key sums over up to 16384 queries of each of the group's 8 heads: two thousand
     64-row steps of one backward CTA, over several query blocks and items. The third case runs
     the backward in query bands of 2048 rows (one launch per band, dK/dV summed over eight
-    bands in float32)."""
+    bands in float32). The fourth runs the head_dim 64 kernels (16/2 heads, both groups), whose
+    dQ^T product reads a zero panel above the 64 channels."""
     L = 16384
-    w = W.Workload(f"causal 16k b={b}", [L], b, 64, 8, 128, max(1, L // b // 2), True, token_cap=2 * b,
+    hq, hkv = (64, 8) if head_dim == 128 else (16, 2)
+    w = W.Workload(f"causal 16k b={b}", [L], b, hq, hkv, head_dim, max(1, L // b // 2), True, token_cap=2 * b,
                    coalesce=c)
     r = U.run_path(fcp, w, bwd_band=band)
     assert r["att"].plan.bwd_bands()[1] == band
     G = w.hq // w.hkv
-    groups = (3, 7)
+    groups = (3, 7) if hkv == 8 else (0, 1)
     q, k, v, do = (r[n].detach().cpu() for n in ("q", "k", "v", "do"))
     # the inputs depend on the seed and the shapes only, so both block sizes share one oracle run
     fingerprint = tuple(float(t.double().sum()) for t in (q, k, v, do))
@@ -283,7 +286,7 @@ def test_backward_long_accumulation_all_key_rows(fcp, b, c, band):
         _LONG_ACC.update(inputs=fingerprint, ref=ref)
     dq, dk, dv = r["grads"]
     for g, (rdq, rdk, rdv) in zip(groups, _LONG_ACC["ref"]):
-        where = f"b={b} c={c} band={band} group {g}"
+        where = f"b={b} c={c} band={band} D={head_dim} group {g}"
         U.check_grad("dk", U.np64(dk[g]), rdk, where)
         U.check_grad("dv", U.np64(dv[g]), rdv, where)
         U.check_grad("dq", U.np64(dq[g * G:(g + 1) * G]), rdq, where)
