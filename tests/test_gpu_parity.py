@@ -252,10 +252,11 @@ def test_causal_mixed_all_rows(fcp):
 _LONG_ACC = {}
 
 
-@pytest.mark.parametrize("b,c,band,head_dim", [(4096, 16, 0, 128), (1024, 1, 0, 128), (4096, 16, 2048, 128),
-                                               (4096, 16, 0, 64)],
-                         ids=["b4096 c16", "b1024 c1", "b4096 c16 bands 2048", "b4096 c16 D64"])
-def test_backward_long_accumulation_all_key_rows(fcp, b, c, band, head_dim):
+@pytest.mark.parametrize("b,c,band,head_dim,causal", [(4096, 16, 0, 128, True), (1024, 1, 0, 128, True),
+                                                      (4096, 16, 2048, 128, True), (4096, 16, 0, 64, True),
+                                                      (4096, 16, 0, 128, False)],
+                         ids=["b4096 c16", "b1024 c1", "b4096 c16 bands 2048", "b4096 c16 D64", "full mask b4096 c16"])
+def test_backward_long_accumulation_all_key_rows(fcp, b, c, band, head_dim, causal):
     """dK and dV of every key row, and dQ of every query row, of two KV-head groups of a
     16384-token causal sequence (64/8 heads, D = 128) against the oracle's whole-group
     gradient: at 4096-token blocks with coalesce degree 16 (the benchmark's launch
@@ -264,29 +265,30 @@ def test_backward_long_accumulation_all_key_rows(fcp, b, c, band, head_dim):
     64-row steps of one backward CTA, over several query blocks and items. The third case runs
     the backward in query bands of 2048 rows (one launch per band, dK/dV summed over eight
     bands in float32). The fourth runs the head_dim 64 kernels (16/2 heads, both groups), whose
-    dQ^T product reads a zero panel above the 64 channels."""
+    dQ^T product reads a zero panel above the 64 channels. The fifth drops the causal mask:
+    every key's gradient then sums over all 16384 queries (256 steps per head)."""
     L = 16384
     hq, hkv = (64, 8) if head_dim == 128 else (16, 2)
-    w = W.Workload(f"causal 16k b={b}", [L], b, hq, hkv, head_dim, max(1, L // b // 2), True, token_cap=2 * b,
-                   coalesce=c)
+    w = W.Workload(f"{'causal' if causal else 'full'} 16k b={b}", [L], b, hq, hkv, head_dim, max(1, L // b // 2),
+                   causal, token_cap=2 * b, coalesce=c)
     r = U.run_path(fcp, w, bwd_band=band)
     assert r["att"].plan.bwd_bands()[1] == band
     G = w.hq // w.hkv
     groups = (3, 7) if hkv == 8 else (0, 1)
     q, k, v, do = (r[n].detach().cpu() for n in ("q", "k", "v", "do"))
     # the inputs depend on the seed and the shapes only, so both block sizes share one oracle run
-    fingerprint = tuple(float(t.double().sum()) for t in (q, k, v, do))
+    fingerprint = (causal,) + tuple(float(t.double().sum()) for t in (q, k, v, do))
     if _LONG_ACC.get("inputs") != fingerprint:
         f = lambda t: t.float().numpy()  # noqa: E731
         with OP.pool(len(groups), gb_per_task=8.0) as p:
             ref = p.map(OP.group_backward_task,
-                        [(f(q[g * G:(g + 1) * G]), f(k[g]), f(v[g]), f(do[g * G:(g + 1) * G]), True)
+                        [(f(q[g * G:(g + 1) * G]), f(k[g]), f(v[g]), f(do[g * G:(g + 1) * G]), causal)
                          for g in groups])
         _LONG_ACC.clear()
         _LONG_ACC.update(inputs=fingerprint, ref=ref)
     dq, dk, dv = r["grads"]
     for g, (rdq, rdk, rdv) in zip(groups, _LONG_ACC["ref"]):
-        where = f"b={b} c={c} band={band} D={head_dim} group {g}"
+        where = f"b={b} c={c} band={band} D={head_dim} causal={causal} group {g}"
         U.check_grad("dk", U.np64(dk[g]), rdk, where)
         U.check_grad("dv", U.np64(dv[g]), rdv, where)
         U.check_grad("dq", U.np64(dq[g * G:(g + 1) * G]), rdq, where)
