@@ -507,8 +507,12 @@ def e2e(torch, fcp, w, args, dev, stream, step, flush):
     so step i+1's plan upload does not touch the image step i reads), so step i+1's inputs
     arrive and step i's results leave while step i computes; dO travels during step i's
     forward and O, LSE during its backward. Every step's planning, flush and copies are inside
-    the timed region. `serial` is the same loop with every copy on the compute stream."""
+    the timed region. `serial` is the same loop with every copy on the compute stream. Under
+    several ranks each replica runs this loop after a barrier; the value is every rank's work
+    over the slowest rank's time and the byte counts are summed over the ranks, as for the
+    headline value."""
     hq, hkv, T, D = w.hq, w.hkv, w.total_tokens, w.head_dim
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     hin = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.do)]
     outs = (step.o, step.lse, step.dq, step.dk, step.dv)
     hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(2)]
@@ -569,6 +573,8 @@ def e2e(torch, fcp, w, args, dev, stream, step, flush):
         for i in range(args.warmup):
             one(i)
         torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         h2d.wait_event(e0)
@@ -582,19 +588,21 @@ def e2e(torch, fcp, w, args, dev, stream, step, flush):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / args.steps
 
-    ms = timed(pipelined)
-    ms_serial = timed(serial)
+    # whole job, as the headline value: every rank's steps over the slowest rank's time
+    ms = max_over_ranks(timed(pipelined), dev)
+    ms_serial = max_over_ranks(timed(serial), dev)
     for a in att:
         if fcp.device_error(a.d_plan, stream):
             raise RuntimeError("device error word set in the end-to-end run")
     flops = step.fwd_flops + step.bwd_flops
-    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
-            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout[0]),
+    return {"value": round(whole_job_tflops(flops, world, ms), 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": world * sum(t.numel() * t.element_size() for t in hin),
+            "d2h_bytes_per_step": world * sum(t.numel() * t.element_size() for t in hout[0]),
             "per_step": "plan rebuilt on the host and uploaded, L2 flushed, inputs copied in, results copied out",
             "copies": "h2d and d2h streams, double-buffered: step i+1's inputs and step i's results "
                       "move while step i computes",
-            "serial": {"value": round(flops / (ms_serial * 1e-3) / 1e12, 2), "ms_per_step": round(ms_serial, 3)}}
+            "serial": {"value": round(whole_job_tflops(flops, world, ms_serial), 2),
+                       "ms_per_step": round(ms_serial, 3)}}
 
 
 SWEEP_RUNS = 20  # timed runs per sweep point (the median is reported)
